@@ -1,0 +1,387 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE routing hot path on GB300: route -> dispatch -> permute -> combine.
+
+One step = one pass of the whole path over one batch of synthetic tokens
+(default workload n2048_h1024_e64_k2: N=2048, H=1024, E=64, K=2), inputs
+resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then K timed steps.  Before every timed step
+a 256 MiB buffer is written to flush the 129 MB L2; each step is bracketed by
+CUDA events on the launching stream (the flush is outside the brackets), and
+every kernel of the step has its own event pair.  Under torchrun each rank
+runs its own replica on its own token batch (weak scaling, no collective on
+the data path); the reported time is the max over ranks.
+
+--impl reference times the CPU oracle (oracle/, fp64 C) on the same workload on
+this machine's host cores: the only other implementation of this path here.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "route+dispatch+combine tokens/s on 1 GB300; % of HBM roofline per kernel"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default=mi.BENCH_WORKLOAD, choices=sorted(mi.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- algorithmic bytes per launch
+
+def kernel_bytes(w: mi.Workload):
+    N, H, E, K = w.N, w.H, w.E, w.K
+    route = N * 2 * H + H * E * 2 + N * K * 8 + (E * 4 if w.skew else 0)
+    meta = N * K * 4 * 3                      # read topk_idx, write row_map and src_slot
+    permute = N * 2 * H + N * K * 2 * H + N * K * 4
+    if w.fp8:
+        permute += N * K * H + N * K * (H // 128) * 4
+    combine = N * K * 2 * H + N * 2 * H + N * K * 8
+    return {"route": route, "dispatch_meta": meta, "permute": permute, "combine": combine}
+
+
+# ----------------------------------------------------------------- clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-i={self.gpu}", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for name, val in zip(names, r[3][5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ----------------------------------------------------------------- CPU oracle baseline
+
+def oracle_pass(oracle, Xb, Wb, bias, w: mi.Workload, Y):
+    """One pass of the oracle over the workload: route, dispatch, permute, combine."""
+    idx, tw = oracle.route(Xb, Wb, bias, w.K, w.renorm)
+    counts, offsets, row_map, src_slot = oracle.dispatch(idx, w.E)
+    oracle.permute(Xb, row_map, w.K, fp8=w.fp8)
+    oracle.combine(Y, row_map, tw)
+    return idx
+
+
+def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000):
+    import oracle
+    X, W, bias = mi.make_workload_inputs(w)
+    Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
+    b = None if bias is None else bias.numpy()
+    r = oracle.run_path(Xb, Wb, b, w.K, w.renorm, w.fp8)   # untimed: provides the expert outputs Y
+    Y = r["Y"]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_pass(oracle, Xb, Wb, b, w, Y)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= max_reps:
+            break
+    return {"value": reps * w.N / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"the whole {w.name} workload ({w.N} tokens), {reps} passes of route+dispatch+permute+"
+                      f"combine in fp64 C, {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    w = mi.WORKLOADS[args.workload]
+    X, W, bias = mi.make_workload_inputs(w)
+    Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
+    b = None if bias is None else bias.numpy()
+    Y = oracle.run_path(Xb, Wb, b, w.K, w.renorm, w.fp8)["Y"]
+    for _ in range(args.warmup):
+        oracle_pass(oracle, Xb, Wb, b, w, Y)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(oracle, Xb, Wb, b, w, Y)
+    el = time.perf_counter() - t0
+    value = args.steps * w.N / el
+    sample = f"the whole {w.name} workload ({w.N} tokens) per step, fp64 C oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": w.as_dict(),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- the GPU arm
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import combine_moe_route_02_gb300 as moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    moe.build()
+    moe.lib()
+
+    w = mi.WORKLOADS[args.workload]
+    X, W, bias = mi.make_route_inputs(w.N, w.H, w.E, seed=rank, skew=w.skew)  # each rank its own tokens
+    Xd, Wd = X.to(dev), W.to(dev)
+    bd = None if bias is None else bias.to(dev)
+    N, H, E, K = w.N, w.H, w.E, w.K
+
+    idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    tw = torch.empty((N, K), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    d = moe.dispatch(moe.route(Xd, Wd, K, bd, w.renorm, topk_idx=idx, topk_w=tw)[0], E, Xd, fp8=w.fp8)
+    # expert outputs for the combine: synthetic stand-in built once (untimed)
+    expert = torch.repeat_interleave(torch.arange(E, device=dev), d.expert_counts.to(torch.int64))
+    scale = torch.tensor([np.float32(1.0 + e / E) for e in range(E)], dtype=torch.float32, device=dev)
+    Y = (d.X_perm.float() * scale[expert][:, None]).to(torch.bfloat16)
+    out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # The timed loop calls the C ABI directly with pointers marshalled once, so
+    # that host-side Python work stays far below the GPU time of a step.
+    L = moe.lib()
+    vp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    route_args = (vp(Xd), vp(Wd), vp(bd), N, H, E, K, int(w.renorm), vp(idx), vp(tw), vp(st), moe.ROUTE_AUTO, sp)
+    meta_args = (vp(idx), None, N, H, E, K, vp(d.expert_counts), vp(d.expert_offsets), vp(d.row_map),
+                 vp(d.src_slot), None, None, None, vp(st), None, 0, sp)
+    perm_args = (vp(Xd), vp(d.row_map), N, H, K, vp(d.X_perm), vp(d.X_fp8), vp(d.X_scale), vp(st), sp)
+    comb_args = (vp(Y), vp(d.row_map), vp(tw), N, H, K, vp(out), vp(st), sp)
+
+    def step(ev=None):
+        rc = 0
+        if ev is not None:
+            ev[0].record(stream)
+        rc |= L.moe_route_ex(*route_args)
+        if ev is not None:
+            ev[1].record(stream)
+        rc |= L.moe_dispatch(*meta_args)           # counting-sort metadata
+        if ev is not None:
+            ev[2].record(stream)
+        rc |= L.moe_permute(*perm_args)            # row permute (+ E4M3)
+        if ev is not None:
+            ev[3].record(stream)
+        rc |= L.moe_combine(*comb_args)
+        if ev is not None:
+            ev[4].record(stream)
+        if rc:
+            raise RuntimeError(f"a library call failed: {moe.status_string(rc)}")
+
+    kernels_per_step = 4
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert st.item() == 0, moe.status_string(st.item())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t1 = time.time()
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+    assert st.item() == 0, moe.status_string(st.item())
+
+    names = ["route", "dispatch_meta", "permute", "combine"]
+    per = {n: [] for n in names}
+    step_ms = []
+    for ev in evs:
+        for j, n in enumerate(names):
+            per[n].append(ev[j].elapsed_time(ev[j + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[4]))
+    total_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * N * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API: pinned host X in, host out back, every step
+    Xh = X.pin_memory()
+    outh = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        Xd.copy_(Xh, non_blocking=True)
+        step()
+        outh.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.e2e_steps):
+        flush.zero_()
+        e0.record(stream)
+        Xd.copy_(Xh, non_blocking=True)
+        step()
+        outh.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_mean = statistics.fmean(e2e_ms)
+    if pg:
+        t = torch.tensor([e2e_mean], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_mean = float(t.item())
+
+    if rank != 0:
+        pg.destroy_process_group()
+        return
+
+    peak, peak_src = measured_peaks()
+    kb = kernel_bytes(w)
+    kern = {}
+    for n in names:
+        ms = statistics.fmean(per[n])
+        kern[n] = {"ms": ms, "algorithmic_bytes": kb[n], "gbs": kb[n] / (ms * 1e-3) / 1e9,
+                   "frac_of_" + peak_src + "_hbm": kb[n] / (ms * 1e-3) / 1e9 / peak}
+    dom = max(names, key=lambda n: kern[n]["ms"])
+    roof = {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
+            "frac": kern[dom]["gbs"] / peak, "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_src == "measured" else "fallback 6800 GB/s",
+            "traffic": None, "algorithmic_bytes_per_launch": kb[dom]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(w.as_dict(), l2="256 MiB buffer written before every timed step (L2 flush)",
+                       accumulate="fp32", parallelism="replicas: each GPU routes its own tokens, no collective"),
+        "roofline": roof, "kernels": kern, "gpu_launches": kernels_per_step * args.steps,
+        "e2e": {"value": world * N / (e2e_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": N * H * 2,
+                "d2h_bytes_per_step": N * H * 2, "ms_per_step": e2e_mean,
+                "path": "pinned host X -> device, route, dispatch, permute, combine, out -> pinned host"},
+        "clocks": sampler.summary(t0, t1) if sampler else None,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+"""GB300 (sm_103a) MoE routing hot path: route -> dispatch -> permute -> combine.
+
+A thin ctypes binding over the C ABI of ``libmoe_route_gb300.so`` (declared in
+``include/moe_route.h``).  This module only marshals arguments: it checks
+dtypes, devices and contiguity, allocates outputs with torch when the caller
+does not pass them, and hands raw device pointers plus the current CUDA stream
+to the library.  Every step of the path runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback -- if the library is missing the calls
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "build", "lib", "MoeError", "route", "dispatch", "permute", "combine",
+    "dispatch_workspace_size", "status_string", "ROUTE_AUTO", "ROUTE_TCGEN05", "ROUTE_SIMT",
+    "Dispatch",
+]
+
+MOE_OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_MISALIGNED = 3
+ERR_WORKSPACE = 4
+ERR_CUDA = 5
+ERR_TIMEOUT = 6
+ERR_BAD_INDEX = 7
+
+ROUTE_AUTO = 0
+ROUTE_TCGEN05 = 1
+ROUTE_SIMT = 2
+_ALGOS = {"auto": ROUTE_AUTO, "tcgen05": ROUTE_TCGEN05, "simt": ROUTE_SIMT}
+
+ABI_VERSION = 1
+EXPORTED_SYMBOLS = (
+    "moe_route", "moe_route_ex", "moe_dispatch_workspace_size", "moe_dispatch",
+    "moe_permute", "moe_combine", "moe_status_string", "moe_abi_version",
+)
+
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a) and return its path."""
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded shared library (ctypes.CDLL) with argument types set."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB_PATH):
+        raise RuntimeError(
+            f"CUDA library {_build.LIB_PATH} is not built; run combine_moe_route_02_gb300.build() "
+            "(there is no CPU fallback)")
+    L = ctypes.CDLL(_build.LIB_PATH)
+    P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.moe_route.argtypes = [P, P, P, I64, I32, I32, I32, I32, P, P, P, P]
+    L.moe_route.restype = I32
+    L.moe_route_ex.argtypes = [P, P, P, I64, I32, I32, I32, I32, P, P, P, I32, P]
+    L.moe_route_ex.restype = I32
+    L.moe_dispatch_workspace_size.argtypes = [I64, I32, I32]
+    L.moe_dispatch_workspace_size.restype = SZ
+    L.moe_dispatch.argtypes = [P, P, I64, I32, I32, I32, P, P, P, P, P, P, P, P, P, SZ, P]
+    L.moe_dispatch.restype = I32
+    L.moe_permute.argtypes = [P, P, I64, I32, I32, P, P, P, P, P]
+    L.moe_permute.restype = I32
+    L.moe_combine.argtypes = [P, P, P, I64, I32, I32, P, P, P]
+    L.moe_combine.restype = I32
+    L.moe_status_string.argtypes = [I32]
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_abi_version.argtypes = []
+    L.moe_abi_version.restype = I32
+    if L.moe_abi_version() != ABI_VERSION:
+        raise RuntimeError("libmoe_route_gb300.so ABI version mismatch; rebuild it")
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().moe_status_string(int(code)).decode()
+    except RuntimeError:
+        return f"moe_status {code}"
+
+
+def _check(code: int, where: str):
+    if code != MOE_OK:
+        raise MoeError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def route(X: torch.Tensor, W_gate: torch.Tensor, K: int, bias: Optional[torch.Tensor] = None,
+          renorm: bool = True, algo: str = "auto", topk_idx=None, topk_w=None, status=None,
+          stream=None):
+    """Fused router: returns (topk_idx int32 [N,K], topk_w fp32 [N,K])."""
+    N, H = X.shape
+    E = W_gate.shape[1]
+    _need(X, "X", torch.bfloat16)
+    _need(W_gate, "W_gate", torch.bfloat16, (H, E))
+    if bias is not None:
+        _need(bias, "bias", torch.float32, (E,))
+    if topk_idx is None:
+        topk_idx = torch.empty((N, K), dtype=torch.int32, device=X.device)
+    if topk_w is None:
+        topk_w = torch.empty((N, K), dtype=torch.float32, device=X.device)
+    _need(topk_idx, "topk_idx", torch.int32, (N, K))
+    _need(topk_w, "topk_w", torch.float32, (N, K))
+    code = lib().moe_route_ex(_ptr(X), _ptr(W_gate), _ptr(bias), N, H, E, K, int(bool(renorm)),
+                              _ptr(topk_idx), _ptr(topk_w), _ptr(status), _ALGOS[algo], _stream(stream))
+    _check(code, "moe_route")
+    return topk_idx, topk_w
+
+
+@dataclass
+class Dispatch:
+    expert_counts: torch.Tensor
+    expert_offsets: torch.Tensor
+    row_map: torch.Tensor
+    src_slot: Optional[torch.Tensor]
+    X_perm: Optional[torch.Tensor] = None
+    X_fp8: Optional[torch.Tensor] = None
+    X_scale: Optional[torch.Tensor] = None
+
+
+def dispatch_workspace_size(N: int, E: int, K: int) -> int:
+    return int(lib().moe_dispatch_workspace_size(N, E, K))
+
+
+def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, fp8: bool = False,
+             bf16: bool = True, want_src_slot: bool = True, out: Optional[Dispatch] = None,
+             workspace: Optional[torch.Tensor] = None, status=None, stream=None) -> Dispatch:
+    """Counting-sort dispatch (+ optional row permute / E4M3 quantise)."""
+    N, K = topk_idx.shape
+    _need(topk_idx, "topk_idx", torch.int32)
+    dev = topk_idx.device
+    H = 0
+    if X is not None:
+        _need(X, "X", torch.bfloat16)
+        if X.shape[0] != N:
+            raise ValueError("X and topk_idx disagree on N")
+        H = X.shape[1]
+    if out is None:
+        out = Dispatch(
+            expert_counts=torch.empty(E, dtype=torch.int32, device=dev),
+            expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            row_map=torch.empty(N * K, dtype=torch.int32, device=dev),
+            src_slot=torch.empty(N * K, dtype=torch.int32, device=dev) if want_src_slot else None,
+            X_perm=torch.empty((N * K, H), dtype=torch.bfloat16, device=dev) if (X is not None and bf16) else None,
+            X_fp8=torch.empty((N * K, H), dtype=torch.uint8, device=dev) if (X is not None and fp8) else None,
+            X_scale=torch.empty((N * K, H // 128), dtype=torch.float32, device=dev)
+            if (X is not None and fp8) else None,
+        )
+    ws_bytes = dispatch_workspace_size(N, E, K)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    has_x = X is not None
+    code = lib().moe_dispatch(
+        _ptr(topk_idx), _ptr(X), N, H, E, K, _ptr(out.expert_counts), _ptr(out.expert_offsets),
+        _ptr(out.row_map), _ptr(out.src_slot), _ptr(out.X_perm) if has_x else None,
+        _ptr(out.X_fp8) if has_x else None, _ptr(out.X_scale) if has_x else None,
+        _ptr(status), _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
+    _check(code, "moe_dispatch")
+    return out
+
+
+def permute(X: torch.Tensor, row_map: torch.Tensor, K: int, bf16: bool = True, fp8: bool = False,
+            X_perm=None, X_fp8=None, X_scale=None, status=None, stream=None):
+    """Row permute: returns (X_perm, X_fp8, X_scale) (entries None when not requested)."""
+    N, H = X.shape
+    _need(X, "X", torch.bfloat16)
+    _need(row_map, "row_map", torch.int32, (N * K,))
+    dev = X.device
+    if bf16 and X_perm is None:
+        X_perm = torch.empty((N * K, H), dtype=torch.bfloat16, device=dev)
+    if fp8 and X_fp8 is None:
+        X_fp8 = torch.empty((N * K, H), dtype=torch.uint8, device=dev)
+        X_scale = torch.empty((N * K, H // 128), dtype=torch.float32, device=dev)
+    code = lib().moe_permute(_ptr(X), _ptr(row_map), N, H, K, _ptr(X_perm), _ptr(X_fp8), _ptr(X_scale),
+                             _ptr(status), _stream(stream))
+    _check(code, "moe_permute")
+    return X_perm, X_fp8, X_scale
+
+
+def combine(Y: torch.Tensor, row_map: torch.Tensor, topk_w: torch.Tensor, out=None, status=None,
+            stream=None) -> torch.Tensor:
+    """Weighted gather back to token order: out bf16 [N,H]."""
+    N, K = topk_w.shape
+    H = Y.shape[1]
+    _need(Y, "Y", torch.bfloat16, (N * K, H))
+    _need(row_map, "row_map", torch.int32, (N * K,))
+    _need(topk_w, "topk_w", torch.float32)
+    if out is None:
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=Y.device)
+    _need(out, "out", torch.bfloat16, (N, H))
+    code = lib().moe_combine(_ptr(Y), _ptr(row_map), _ptr(topk_w), N, H, K, _ptr(out), _ptr(status),
+                             _stream(stream))
+    _check(code, "moe_combine")
+    return out

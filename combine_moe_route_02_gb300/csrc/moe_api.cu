@@ -1,0 +1,207 @@
+// moe_api.cu -- the C ABI of the routing library: argument validation on the
+// host (before any CUDA call, so that a rejected call touches no device
+// state), implementation choice, and the launches.
+#include <atomic>
+#include <climits>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_cc_major[kMaxDevices];
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+inline moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_topk(int E, int K)
+{
+    if (E < 1 || E > 256) return MOE_ERR_INVALID_ARG;
+    if (K < 1 || K > 16 || K > E) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status check_rows(int64_t N, int K)
+{
+    if (N < 0) return MOE_ERR_INVALID_ARG;
+    if (N > 0 && N > (static_cast<int64_t>(INT_MAX) - 1) / K) return MOE_ERR_INVALID_ARG;  // N*K < 2^31
+    return MOE_OK;
+}
+}  // namespace
+
+int device_sm_count(int device)
+{
+    const int d = device & (kMaxDevices - 1);
+    int v = g_sm_count[d].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) v = 1;
+        g_sm_count[d].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+int device_cc_major(int device)
+{
+    const int d = device & (kMaxDevices - 1);
+    int v = g_cc_major[d].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess || v <= 0)
+            v = -1;
+        g_cc_major[d].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(moe_status s)
+{
+    switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: a required pointer is NULL or a size is out of range";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: the requested implementation cannot take this shape";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED: pointers must be 16-byte aligned and H a multiple of 8";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace smaller than moe_dispatch_workspace_size()";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait ran out";
+    case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX: an expert index or row index was out of range";
+    }
+    return "unknown moe_status";
+}
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+moe_status moe_route_ex(const void *X, const void *W_gate, const float *bias, int64_t N, int H, int E, int K,
+                        int renorm, int32_t *topk_idx, float *topk_w, int32_t *status_word, int algo,
+                        moe_stream_t stream)
+{
+    moe_status st = check_topk(E, K);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(N, K)) != MOE_OK) return st;
+    if (algo < MOE_ROUTE_AUTO || algo > MOE_ROUTE_SIMT) return MOE_ERR_INVALID_ARG;
+    if (H < 1) return MOE_ERR_INVALID_ARG;
+    if (N == 0) return MOE_OK;
+    if (!X || !W_gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_MISALIGNED;
+    if (!aligned16(X) || !aligned16(W_gate) || !aligned4(topk_idx) || !aligned4(topk_w) ||
+        (bias && !aligned4(bias)) || (status_word && !aligned4(status_word)))
+        return MOE_ERR_MISALIGNED;
+
+    RouteArgs a{X, W_gate, bias, N, H, E, K, renorm ? 1 : 0, topk_idx, topk_w, status_word};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    const bool tc_ok = route_tc_supported(a, dev);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (algo == MOE_ROUTE_TCGEN05 && !tc_ok) return MOE_ERR_UNSUPPORTED;
+    if (algo == MOE_ROUTE_SIMT || !tc_ok) return from_cuda(launch_route_simt(a, s));
+    return from_cuda(launch_route_tc(a, s));
+}
+
+moe_status moe_route(const void *X, const void *W_gate, const float *bias, int64_t N, int H, int E, int K,
+                     int renorm, int32_t *topk_idx, float *topk_w, int32_t *status_word, moe_stream_t stream)
+{
+    return moe_route_ex(X, W_gate, bias, N, H, E, K, renorm, topk_idx, topk_w, status_word, MOE_ROUTE_AUTO,
+                        stream);
+}
+
+size_t moe_dispatch_workspace_size(int64_t N, int E, int K)
+{
+    (void)N;
+    (void)E;
+    (void)K;
+    return 0;  // the cluster counting sort keeps its histograms in shared memory
+}
+
+static moe_status validate_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K,
+                                   const void *X_perm, const void *X_fp8, const float *X_scale)
+{
+    if (!X || !row_map) return MOE_ERR_INVALID_ARG;
+    if (!X_perm && !X_fp8) return MOE_ERR_INVALID_ARG;
+    if ((X_fp8 == nullptr) != (X_scale == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (H < 1) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_MISALIGNED;
+    if (X_fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(X) || (X_perm && !aligned16(X_perm)) || (X_fp8 && !aligned16(X_fp8)) ||
+        (X_scale && !aligned4(X_scale)) || !aligned4(row_map))
+        return MOE_ERR_MISALIGNED;
+    (void)N;
+    (void)K;
+    return MOE_OK;
+}
+
+moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                        int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
+                        void *X_perm, void *X_fp8, float *X_scale, int32_t *status_word, void *workspace,
+                        size_t workspace_bytes, moe_stream_t stream)
+{
+    moe_status st = check_topk(E, K);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(N, K)) != MOE_OK) return st;
+    if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
+    if (!aligned4(expert_counts) || !aligned4(expert_offsets) || (status_word && !aligned4(status_word)))
+        return MOE_ERR_MISALIGNED;
+    if (!X && (X_perm || X_fp8 || X_scale)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < moe_dispatch_workspace_size(N, E, K)) return MOE_ERR_WORKSPACE;
+    (void)workspace;
+    if (N > 0) {
+        if (!topk_idx || !row_map) return MOE_ERR_INVALID_ARG;
+        if (!aligned4(topk_idx) || !aligned4(row_map) || (src_slot && !aligned4(src_slot)))
+            return MOE_ERR_MISALIGNED;
+        if (X && (st = validate_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale)) != MOE_OK) return st;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        // no tokens: every count and offset is zero
+        if (cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    cudaError_t e = launch_dispatch_meta(topk_idx, N, E, K, expert_counts, expert_offsets, row_map, src_slot,
+                                         status_word, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (X) {
+        e = launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, status_word, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm, void *X_fp8,
+                       float *X_scale, int32_t *status_word, moe_stream_t stream)
+{
+    if (K < 1 || K > 16) return MOE_ERR_INVALID_ARG;
+    moe_status st = check_rows(N, K);
+    if (st != MOE_OK) return st;
+    if (N == 0) return MOE_OK;
+    if ((st = validate_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale)) != MOE_OK) return st;
+    if (status_word && !aligned4(status_word)) return MOE_ERR_MISALIGNED;
+    return from_cuda(launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, status_word,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine(const void *Y, const int32_t *row_map, const float *topk_w, int64_t N, int H, int K,
+                       void *out, int32_t *status_word, moe_stream_t stream)
+{
+    if (K < 1 || K > 16) return MOE_ERR_INVALID_ARG;
+    moe_status st = check_rows(N, K);
+    if (st != MOE_OK) return st;
+    if (H < 1) return MOE_ERR_INVALID_ARG;
+    if (N == 0) return MOE_OK;
+    if (!Y || !row_map || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_MISALIGNED;
+    if (!aligned16(Y) || !aligned16(out) || !aligned4(row_map) || !aligned4(topk_w) ||
+        (status_word && !aligned4(status_word)))
+        return MOE_ERR_MISALIGNED;
+    return from_cuda(launch_combine(Y, row_map, topk_w, N, H, K, out, status_word,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+/*
+ * moe_route.h -- C ABI of the GB300 (sm_103a) MoE routing library
+ * (libmoe_route_gb300.so): route -> dispatch -> permute -> combine on one GPU.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers to row-major, contiguous
+ *    buffers that the caller owns.  The library allocates and frees nothing,
+ *    keeps no per-call state between calls and may be called from several
+ *    host threads at once (each call only touches its own arguments).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and never synchronises the host, so a sequence
+ *    of calls can be captured into a CUDA graph.
+ *  - Argument errors are found on the host before anything is launched; the
+ *    call then returns a non-zero moe_status and launches nothing.  A failed
+ *    launch returns MOE_ERR_CUDA.
+ *  - Errors that only the device can see (an expert index outside [0,E), a
+ *    bounded wait that ran out) are recorded in `status_word` (one int32 in
+ *    device memory, may be NULL): the first error code is stored with an
+ *    atomic compare-and-swap over 0, so the caller zeroes the word before the
+ *    call and reads it after synchronising.  No kernel traps or asserts.
+ *  - bf16 buffers are passed as `void*` (IEEE bfloat16 bit patterns).
+ *  - Pointers must be 16-byte aligned; H must be a multiple of 8.
+ *
+ * Notation: N tokens, H hidden size, E experts, K experts per token,
+ * slot s = n*K + k.  Limits: 1 <= E <= 256, 1 <= K <= min(E, 16),
+ * N*K < 2^31, N >= 0 (N == 0 is a no-op that returns MOE_OK).
+ */
+#ifndef MOE_ROUTE_GB300_H
+#define MOE_ROUTE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* a NULL required pointer, a size out of range */
+    MOE_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement */
+    MOE_ERR_MISALIGNED = 3,    /* a pointer not 16-byte aligned, H % 8 != 0 */
+    MOE_ERR_WORKSPACE = 4,     /* workspace smaller than moe_dispatch_workspace_size() */
+    MOE_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_TIMEOUT = 6,       /* (status_word only) a bounded device wait ran out */
+    MOE_ERR_BAD_INDEX = 7      /* (status_word only) topk_idx entry outside [0,E) */
+} moe_status;
+
+/* Router implementation selector for moe_route_ex. */
+typedef enum moe_route_algo {
+    MOE_ROUTE_AUTO = 0,        /* tensor-core kernel where the shape allows it */
+    MOE_ROUTE_TCGEN05 = 1,     /* tcgen05.mma + TMEM + TMA kernel (E % 8 == 0) */
+    MOE_ROUTE_SIMT = 2         /* CUDA-core kernel, any E */
+} moe_route_algo;
+
+/*
+ * moe_route -- the fused router.
+ * Defined by the moe-engine page ("moe-engine：面向万卡集群的稀疏MoE训练基础设施"),
+ * section 融合Triton路由内核: tokens @ gate_w -> softmax -> top-K -> renorm,
+ * with K-round selection.  For every token n:
+ *   L[e]   = sum_h X[n,h] * W_gate[h,e] (+ bias[e])    bf16 x bf16, fp32 accumulate
+ *   p[e]   = softmax_e(L)[e]                          fp32
+ *   idx    = the K experts with the largest logits, in descending order;
+ *            equal logits go to the lower expert index; NaN counts as -inf
+ *   w_k    = p[idx_k] / sum_j p[idx_j]  if renorm,  else  p[idx_k]
+ * Arguments:
+ *   X          bf16 [N,H]          token activations (read once)
+ *   W_gate     bf16 [H,E]          gate weight, row-major ("tokens @ gate_w")
+ *   bias       fp32 [E] or NULL    per-expert logit bias added before softmax
+ *   topk_idx   int32 [N,K]         out: selected experts per token
+ *   topk_w     fp32 [N,K]          out: routing weights
+ *   status_word int32 [1] or NULL  device error word (MOE_ERR_TIMEOUT)
+ * Errors: MOE_ERR_INVALID_ARG (NULL X/W_gate/outputs with N > 0, E or K out
+ * of range), MOE_ERR_MISALIGNED, MOE_ERR_CUDA.
+ */
+MOE_API moe_status moe_route(const void *X, const void *W_gate, const float *bias,
+                     int64_t N, int H, int E, int K, int renorm,
+                     int32_t *topk_idx, float *topk_w, int32_t *status_word,
+                     moe_stream_t stream);
+
+/* moe_route with an explicit implementation; MOE_ERR_UNSUPPORTED if the
+ * requested kernel cannot take this shape (MOE_ROUTE_TCGEN05 needs E % 8 == 0
+ * and a GPU of compute capability 10.x). */
+MOE_API moe_status moe_route_ex(const void *X, const void *W_gate, const float *bias,
+                        int64_t N, int H, int E, int K, int renorm,
+                        int32_t *topk_idx, float *topk_w, int32_t *status_word,
+                        int algo, moe_stream_t stream);
+
+/* Bytes of device workspace moe_dispatch needs for these sizes (0 means the
+ * workspace pointer may be NULL). */
+MOE_API size_t moe_dispatch_workspace_size(int64_t N, int E, int K);
+
+/*
+ * moe_dispatch -- counting-sort dispatch into an expert-contiguous buffer.
+ * Defined by the PithTrain page ("一万行Python构建MoE训练栈：解构4D并行、
+ * DualPipeV调度与FP8算子"), §8.2 O(n) counting sort 替代 O(n log n) argsort
+ * (bincount with private histograms -> prefix sum -> scatter with
+ * expand_idx), specialised to one GPU (no expert-parallel ranks, no
+ * all-to-all), and by the moe-engine page's conservation check
+ * sum(dispatch_cnt) == N*K (section 实验结果与性能数据 / Token守恒验证).
+ *   expert_counts[e]  = #{slots s : topk_idx[s] == e}
+ *   expert_offsets[e] = sum_{e' < e} expert_counts[e'],  expert_offsets[E] = N*K
+ *   row_map[s]        = the row of slot s in the expert-contiguous buffer;
+ *                       rows are ordered by (expert, s): the stable argsort
+ *                       of the slots by expert
+ *   src_slot[r]       = the slot whose row is r (inverse of row_map)
+ * and, when X is given, the row permute of moe_permute below.
+ * Arguments:
+ *   topk_idx        int32 [N,K]     expert ids (from moe_route or the caller)
+ *   X               bf16 [N,H] or NULL   NULL: metadata only
+ *   expert_counts   int32 [E]       out
+ *   expert_offsets  int32 [E+1]     out
+ *   row_map         int32 [N*K]     out
+ *   src_slot        int32 [N*K] or NULL   out
+ *   X_perm          bf16 [N*K,H] or NULL  out (needs X)
+ *   X_fp8           uint8 [N*K,H] or NULL out, E4M3 codes (needs X, H % 128 == 0)
+ *   X_scale         fp32 [N*K,H/128] or NULL  out, with X_fp8
+ *   status_word     int32 [1] or NULL  device error word (MOE_ERR_BAD_INDEX)
+ *   workspace       device scratch of moe_dispatch_workspace_size() bytes
+ * An index outside [0,E) is reported in status_word; the outputs are then
+ * unspecified but every write stays inside the buffers described above.
+ */
+MOE_API moe_status moe_dispatch(const int32_t *topk_idx, const void *X,
+                        int64_t N, int H, int E, int K,
+                        int32_t *expert_counts, int32_t *expert_offsets,
+                        int32_t *row_map, int32_t *src_slot,
+                        void *X_perm, void *X_fp8, float *X_scale,
+                        int32_t *status_word,
+                        void *workspace, size_t workspace_bytes,
+                        moe_stream_t stream);
+
+/*
+ * moe_permute -- the row permute of the dispatch, on its own.
+ * The gathered_tokens input of forward_mlp on the PithTrain page
+ * (§6.1 模型协议先行): X_perm[row_map[n*K+k], :] = X[n, :].
+ * With X_fp8/X_scale (H % 128 == 0) every 1x128 block of X[n,:] is also
+ * quantised with the power-of-two scale of §7.2 架构感知的量化核
+ * (_compute_fp8_scale, fp32-scale branch):
+ *   s = pow2ceil(fl32(max(amax, 1e-4) * fl32(1/448))),  q = E4M3_rn_satfinite(x / s)
+ * and q, s are written for every destination row of the token.
+ * row_map must be a permutation of [0, N*K) (as moe_dispatch writes it);
+ * rows outside [0, N*K) are skipped and reported as MOE_ERR_BAD_INDEX.
+ * X_perm may be NULL when only the E4M3 copy is wanted.
+ */
+MOE_API moe_status moe_permute(const void *X, const int32_t *row_map,
+                       int64_t N, int H, int K,
+                       void *X_perm, void *X_fp8, float *X_scale,
+                       int32_t *status_word, moe_stream_t stream);
+
+/*
+ * moe_combine -- weighted gather back to token order.
+ * The weighted part of forward_aggregate on the PithTrain page (§6.1
+ * 模型协议先行, "weighted expert output"):
+ *   out[n,:] = sum_{k=0}^{K-1} topk_w[n,k] * Y[row_map[n*K+k], :]
+ * accumulated in fp32 in k order and rounded to bf16 (nearest even).
+ * Arguments: Y bf16 [N*K,H] (expert outputs in the expert-contiguous order),
+ * row_map int32 [N*K], topk_w fp32 [N,K], out bf16 [N,H].
+ * Rows outside [0, N*K) contribute nothing and are reported as
+ * MOE_ERR_BAD_INDEX in status_word.
+ */
+MOE_API moe_status moe_combine(const void *Y, const int32_t *row_map, const float *topk_w,
+                       int64_t N, int H, int K, void *out,
+                       int32_t *status_word, moe_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+MOE_API const char *moe_status_string(moe_status status);
+
+/* ABI version of this header (bumped on any signature change). */
+MOE_API int moe_abi_version(void);
+#define MOE_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_GB300_H */

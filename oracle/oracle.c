@@ -369,11 +369,14 @@ int oracle_permute(const uint16_t *X, const int32_t *row_map,
     if ((Xq || Xs) && (H % 128 != 0 || !Xq || !Xs))
         return ORACLE_BAD_ARG;
     int64_t nb = H / 128;
+    for (int64_t s = 0; s < N * K; ++s)
+        if (row_map[s] < 0 || row_map[s] >= N * K)
+            return ORACLE_BAD_INDEX;
+    /* tokens are independent (each destination row has one source slot) */
+#pragma omp parallel for schedule(static)
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t k = 0; k < K; ++k) {
             int64_t r = row_map[n * K + k];
-            if (r < 0 || r >= N * K)
-                return ORACLE_BAD_INDEX;
             if (Xp)
                 memcpy(Xp + r * H, X + n * H, sizeof(uint16_t) * (size_t)H);
             if (Xq) {
@@ -445,6 +448,7 @@ int oracle_expert_fixture(const uint16_t *Xp, const int32_t *offsets,
         return ORACLE_BAD_ARG;
     for (int64_t e = 0; e < E; ++e) {
         float f = (float)(1.0 + (double)e / (double)E);
+#pragma omp parallel for schedule(static)
         for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p)
             for (int64_t h = 0; h < H; ++h) {
                 double x = oracle_bf16_to_f64(Xp[p * H + h]);

@@ -1,0 +1,137 @@
+"""The C ABI on the host: the library loads, exports every entry point that
+include/moe_route.h declares, and rejects bad arguments with status codes
+before touching CUDA (so these run on a machine without a GPU; no compute is
+launched, every pointer below is a fake address that is never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import combine_moe_route_02_gb300 as moe
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_route.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA = 0, 1, 2, 3, 4, 5
+
+A = 0x10000   # a 16-byte aligned fake device address
+A2 = 0x20000
+A3 = 0x30000
+A4 = 0x40000
+
+
+@pytest.fixture(scope="module")
+def L():
+    moe.build()
+    return moe.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("moe_route", "moe_dispatch", "moe_combine", "moe_dispatch_workspace_size",
+              "moe_status_string"):
+        assert s in syms
+    assert set(syms) == set(moe.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for s in declared_symbols():
+        assert hasattr(L, s), s
+    assert L.moe_abi_version() == moe.ABI_VERSION
+
+
+def test_status_strings(L):
+    for code in range(8):
+        s = moe.status_string(code)
+        assert s.startswith("MOE_")
+    assert "unknown" in moe.status_string(99)
+
+
+def route(L, X=A, W=A2, bias=None, N=16, H=64, E=16, K=2, idx=A3, w=A4, algo=0):
+    return L.moe_route_ex(X, W, bias, N, H, E, K, 1, idx, w, None, algo, None)
+
+
+def test_route_validation(L):
+    assert route(L, N=0) == OK                     # no tokens: nothing to do
+    assert route(L, E=0) == INVALID
+    assert route(L, E=257) == INVALID
+    assert route(L, K=0) == INVALID
+    assert route(L, K=17, E=32) == INVALID
+    assert route(L, K=5, E=4) == INVALID
+    assert route(L, N=-1) == INVALID
+    assert route(L, X=None) == INVALID
+    assert route(L, idx=None) == INVALID
+    assert route(L, H=0) == INVALID
+    assert route(L, H=12) == MISALIGNED
+    assert route(L, X=A + 8) == MISALIGNED
+    assert route(L, W=A2 + 2) == MISALIGNED
+    assert route(L, algo=7) == INVALID
+    assert route(L, N=2**31, K=1) == INVALID       # N*K must stay below 2^31
+
+
+def dispatch(L, idx=A, X=None, N=16, H=64, E=16, K=2, counts=A2, offsets=A3, row_map=A4,
+             src=None, xp=None, xq=None, xs=None, ws=None, ws_bytes=0):
+    return L.moe_dispatch(idx, X, N, H, E, K, counts, offsets, row_map, src, xp, xq, xs, None,
+                          ws, ws_bytes, None)
+
+
+def test_dispatch_validation(L):
+    assert L.moe_dispatch_workspace_size(1 << 20, 64, 8) == 0
+    assert dispatch(L, E=0) == INVALID
+    assert dispatch(L, K=0) == INVALID
+    assert dispatch(L, counts=None) == INVALID
+    assert dispatch(L, idx=None) == INVALID
+    assert dispatch(L, row_map=None) == INVALID
+    assert dispatch(L, xp=A) == INVALID                           # output rows without X
+    assert dispatch(L, X=A, xp=None) == INVALID                   # X without any output
+    assert dispatch(L, X=A, xp=A2 + 4) == MISALIGNED
+    assert dispatch(L, X=A, H=12, xp=A) == MISALIGNED
+    assert dispatch(L, X=A, H=192, xq=A, xs=None) == INVALID      # fp8 codes need scales
+    assert dispatch(L, X=A, H=192, xq=A, xs=A2) == INVALID        # H % 128 != 0
+    assert dispatch(L, idx=A + 2) == MISALIGNED
+    assert dispatch(L, N=-5) == INVALID
+
+
+def test_permute_and_combine_validation(L):
+    assert L.moe_permute(A, A2, 0, 64, 2, A3, None, None, None, None) == OK
+    assert L.moe_permute(None, A2, 8, 64, 2, A3, None, None, None, None) == INVALID
+    assert L.moe_permute(A, A2, 8, 64, 2, None, None, None, None, None) == INVALID
+    assert L.moe_permute(A, A2, 8, 64, 0, A3, None, None, None, None) == INVALID
+    assert L.moe_permute(A, A2, 8, 64, 2, A3 + 8, None, None, None, None) == MISALIGNED
+    assert L.moe_combine(A, A2, A3, 0, 64, 2, A4, None, None) == OK
+    assert L.moe_combine(None, A2, A3, 8, 64, 2, A4, None, None) == INVALID
+    assert L.moe_combine(A, A2, A3, 8, 64, 17, A4, None, None) == INVALID
+    assert L.moe_combine(A, A2, A3, 8, 60, 2, A4, None, None) == MISALIGNED
+    assert L.moe_combine(A, A2, A3, 8, 64, 2, A4 + 8, None, None) == MISALIGNED
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_call_without_gpu_fails_loudly(L):
+    # arguments pass validation, then the first CUDA call fails: MOE_ERR_CUDA, no crash
+    assert route(L) == CUDA
+    assert L.moe_combine(A, A2, A3, 8, 64, 2, A4, None, None) == CUDA
+
+
+def test_binding_refuses_cpu_tensors():
+    X = torch.zeros(4, 64, dtype=torch.bfloat16)
+    W = torch.zeros(64, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        moe.route(X, W, 2)
+
+
+def test_product_does_not_import_oracle():
+    # the product path (package + CUDA sources) never imports, links or loads the oracle
+    here = os.path.dirname(moe.__file__)
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle|#include\s+.*oracle)|_oracle\.so", re.M)
+    for root, _, files in os.walk(here):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f), errors="ignore").read()
+                assert not pat.search(text), f
