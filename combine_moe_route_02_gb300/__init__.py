@@ -21,7 +21,7 @@ from . import _build
 
 __all__ = [
     "build", "lib", "MoeError", "route", "dispatch", "permute", "combine",
-    "dispatch_workspace_size", "status_string", "ROUTE_AUTO", "ROUTE_TCGEN05", "ROUTE_SIMT",
+    "dispatch_workspace_size", "dispatch_workspace", "status_string", "ROUTE_AUTO", "ROUTE_TCGEN05", "ROUTE_SIMT",
     "Dispatch",
 ]
 
@@ -165,10 +165,37 @@ def dispatch_workspace_size(N: int, E: int, K: int) -> int:
     return int(lib().moe_dispatch_workspace_size(N, E, K))
 
 
+_workspaces = {}
+
+
+def dispatch_workspace(E: int, device=None, stream=None) -> torch.Tensor:
+    """A zeroed workspace for moe_dispatch, cached per (device, stream, E).
+
+    The library keeps grid-barrier counters in it: they must start at zero and
+    every completed call leaves them at zero, so one workspace serves any
+    number of calls issued on one stream (calls that overlap on the GPU must
+    not share a workspace)."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    key = (device.index, stream.cuda_stream, E)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.zeros(dispatch_workspace_size(0, E, 1), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
 def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, fp8: bool = False,
              bf16: bool = True, want_src_slot: bool = True, out: Optional[Dispatch] = None,
-             workspace: Optional[torch.Tensor] = None, status=None, stream=None) -> Dispatch:
-    """Counting-sort dispatch (+ optional row permute / E4M3 quantise)."""
+             workspace: Optional[torch.Tensor] = None, fused: bool = True, status=None,
+             stream=None) -> Dispatch:
+    """Counting-sort dispatch (+ optional row permute / E4M3 quantise).
+
+    fused=True (default) runs the one-launch cooperative kernel with a
+    workspace (a cached zeroed one unless given); fused=False passes no
+    workspace, which selects the single-cluster metadata kernel followed by
+    the permute kernel."""
     N, K = topk_idx.shape
     _need(topk_idx, "topk_idx", torch.int32)
     dev = topk_idx.device
@@ -189,9 +216,10 @@ def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, f
             X_scale=torch.empty((N * K, H // 128), dtype=torch.float32, device=dev)
             if (X is not None and fp8) else None,
         )
-    ws_bytes = dispatch_workspace_size(N, E, K)
-    if ws_bytes and workspace is None:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if not fused:
+        workspace = None
+    elif workspace is None:
+        workspace = dispatch_workspace(E, dev, stream)
     has_x = X is not None
     code = lib().moe_dispatch(
         _ptr(topk_idx), _ptr(X), N, H, E, K, _ptr(out.expert_counts), _ptr(out.expert_offsets),

@@ -35,8 +35,10 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8])
     return o;
 }
 
-// KT > 0: K known at compile time (loads of all K rows unrolled); KT == 0: runtime K.
-template <int KT>
+// KT > 0: K known at compile time -- every lane issues the loads of CPL
+// chunks x KT rows before the first FMA (CPL * KT <= 16 uint4 in flight per
+// lane).  KT == 0: runtime K, one chunk at a time.
+template <int KT, int CPL>
 __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
     const uint4 *__restrict__ Y, const int32_t *__restrict__ row_map, const float *__restrict__ w, int64_t N,
     int H, int K_rt, uint4 *__restrict__ out, int32_t *status)
@@ -65,30 +67,27 @@ __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
         }
         uint4 *dst = out + n * chunks;
         if constexpr (KT > 0) {
-            int r[KT];
+            const uint4 *yr[KT];
             float wk[KT];
 #pragma unroll
             for (int k = 0; k < KT; ++k) {
-                r[k] = __shfl_sync(0xffffffffu, my_row, k);
+                yr[k] = Y + static_cast<int64_t>(__shfl_sync(0xffffffffu, my_row, k)) * chunks;
                 wk[k] = __shfl_sync(0xffffffffu, my_w, k);
             }
-            constexpr int U = KT <= 2 ? 4 : (KT <= 4 ? 2 : 1);
-            for (int c0 = lane; c0 < chunks; c0 += 32 * U) {
-                uint4 y[U][KT];
+            for (int base = 0; base < chunks; base += 32 * CPL) {
+                uint4 y[CPL][KT];
 #pragma unroll
-                for (int u = 0; u < U; ++u)
+                for (int j = 0; j < CPL; ++j) {
+                    const int c = base + lane + 32 * j;
 #pragma unroll
-                    for (int k = 0; k < KT; ++k) {
-                        const int c = c0 + 32 * u;
-                        y[u][k] = c < chunks ? __ldcs(Y + static_cast<int64_t>(r[k]) * chunks + c)
-                                             : make_uint4(0, 0, 0, 0);
-                    }
+                    for (int k = 0; k < KT; ++k) y[j][k] = c < chunks ? __ldcs(yr[k] + c) : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = c0 + 32 * u;
+                for (int j = 0; j < CPL; ++j) {
+                    const int c = base + lane + 32 * j;
                     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int k = 0; k < KT; ++k) fma_bf16x8(acc, y[u][k], wk[k]);
+                    for (int k = 0; k < KT; ++k) fma_bf16x8(acc, y[j][k], wk[k]);
                     if (c < chunks) __stcs(dst + c, pack_bf16x8(acc));
                 }
             }
@@ -108,6 +107,13 @@ __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
     }
     if (bad) report_status(status, MOE_ERR_BAD_INDEX);
     pdl_launch_dependents();
+}
+
+int pow2_chunks_per_lane(int chunks, int cap)
+{
+    int c = 1;
+    while (c < cap && 32 * c < chunks) c <<= 1;
+    return c;
 }
 
 }  // namespace
@@ -132,13 +138,39 @@ cudaError_t launch_combine(const void *Y, const int32_t *row_map, const float *w
     cfg.numAttrs = 1;
     const uint4 *y = static_cast<const uint4 *>(Y);
     uint4 *o = static_cast<uint4 *>(out);
+    const int chunks = H / 8;
+#define MOE_COMBINE_LAUNCH(KK, C) \
+    return cudaLaunchKernelEx(&cfg, combine_kernel<KK, C>, y, row_map, w, N, H, K, o, status)
     switch (K) {
-    case 1: return cudaLaunchKernelEx(&cfg, combine_kernel<1>, y, row_map, w, N, H, K, o, status);
-    case 2: return cudaLaunchKernelEx(&cfg, combine_kernel<2>, y, row_map, w, N, H, K, o, status);
-    case 4: return cudaLaunchKernelEx(&cfg, combine_kernel<4>, y, row_map, w, N, H, K, o, status);
-    case 8: return cudaLaunchKernelEx(&cfg, combine_kernel<8>, y, row_map, w, N, H, K, o, status);
-    default: return cudaLaunchKernelEx(&cfg, combine_kernel<0>, y, row_map, w, N, H, K, o, status);
+    case 1:
+        switch (pow2_chunks_per_lane(chunks, 16)) {
+        case 1: MOE_COMBINE_LAUNCH(1, 1);
+        case 2: MOE_COMBINE_LAUNCH(1, 2);
+        case 4: MOE_COMBINE_LAUNCH(1, 4);
+        case 8: MOE_COMBINE_LAUNCH(1, 8);
+        default: MOE_COMBINE_LAUNCH(1, 16);
+        }
+    case 2:
+        switch (pow2_chunks_per_lane(chunks, 8)) {
+        case 1: MOE_COMBINE_LAUNCH(2, 1);
+        case 2: MOE_COMBINE_LAUNCH(2, 2);
+        case 4: MOE_COMBINE_LAUNCH(2, 4);
+        default: MOE_COMBINE_LAUNCH(2, 8);
+        }
+    case 4:
+        switch (pow2_chunks_per_lane(chunks, 4)) {
+        case 1: MOE_COMBINE_LAUNCH(4, 1);
+        case 2: MOE_COMBINE_LAUNCH(4, 2);
+        default: MOE_COMBINE_LAUNCH(4, 4);
+        }
+    case 8:
+        switch (pow2_chunks_per_lane(chunks, 2)) {
+        case 1: MOE_COMBINE_LAUNCH(8, 1);
+        default: MOE_COMBINE_LAUNCH(8, 2);
+        }
+    default: MOE_COMBINE_LAUNCH(0, 1);
     }
+#undef MOE_COMBINE_LAUNCH
 }
 
 }  // namespace moe

@@ -115,9 +115,9 @@ moe_status moe_route(const void *X, const void *W_gate, const float *bias, int64
 size_t moe_dispatch_workspace_size(int64_t N, int E, int K)
 {
     (void)N;
-    (void)E;
     (void)K;
-    return 0;  // the cluster counting sort keeps its histograms in shared memory
+    if (E < 1 || E > 256) return 0;
+    return fused_workspace_bytes(E);  // grid-barrier counters + one count per (CTA, expert)
 }
 
 static moe_status validate_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K,
@@ -149,8 +149,10 @@ moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H
     if (!aligned4(expert_counts) || !aligned4(expert_offsets) || (status_word && !aligned4(status_word)))
         return MOE_ERR_MISALIGNED;
     if (!X && (X_perm || X_fp8 || X_scale)) return MOE_ERR_INVALID_ARG;
-    if (workspace_bytes < moe_dispatch_workspace_size(N, E, K)) return MOE_ERR_WORKSPACE;
-    (void)workspace;
+    // no workspace at all selects the single-cluster path; otherwise it must be large enough
+    const bool use_ws = workspace != nullptr || workspace_bytes != 0;
+    if (use_ws && (!workspace || workspace_bytes < moe_dispatch_workspace_size(N, E, K))) return MOE_ERR_WORKSPACE;
+    if (use_ws && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MOE_ERR_MISALIGNED;
     if (N > 0) {
         if (!topk_idx || !row_map) return MOE_ERR_INVALID_ARG;
         if (!aligned4(topk_idx) || !aligned4(row_map) || (src_slot && !aligned4(src_slot)))
@@ -163,6 +165,13 @@ moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H
         if (cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
         return MOE_OK;
+    }
+    if (use_ws) {
+        const cudaError_t f = launch_dispatch_fused(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map,
+                                                    src_slot, X_perm, X_fp8, X_scale, status_word, workspace,
+                                                    workspace_bytes, s);
+        if (f == cudaSuccess) return MOE_OK;
+        if (f != cudaErrorNotSupported) return MOE_ERR_CUDA;
     }
     cudaError_t e = launch_dispatch_meta(topk_idx, N, E, K, expert_counts, expert_offsets, row_map, src_slot,
                                          status_word, s);

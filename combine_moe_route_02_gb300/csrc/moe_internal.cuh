@@ -74,13 +74,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false) when
 // *abort becomes non-zero or after kWaitLimitNs, in which case it raises
-// *abort itself so that every other role of the CTA stops too.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort)
+// *abort itself so that every other role of the CTA stops too.  sleep_ns > 0
+// parks the thread between polls (for waits that are not latency critical,
+// so that pollers leave issue slots to the producer and MMA warps).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                  uint32_t sleep_ns = 0)
 {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
+        if (sleep_ns) __nanosleep(sleep_ns);
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
@@ -197,9 +201,27 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Named barrier over `count` threads (id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Shared-memory matrix descriptor for tcgen05.mma (sm_100 family format):
@@ -266,6 +288,15 @@ cudaError_t launch_route_simt(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_dispatch_meta(const int32_t *topk_idx, int64_t N, int E, int K, int32_t *counts,
                                  int32_t *offsets, int32_t *row_map, int32_t *src_slot, int32_t *status,
                                  cudaStream_t stream);
+
+// Counting sort + permute in one cooperative launch; cudaErrorNotSupported when
+// the problem or the workspace does not fit (the caller then falls back to the
+// cluster metadata kernel + launch_permute).
+cudaError_t launch_dispatch_fused(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                                  int32_t *counts, int32_t *offsets, int32_t *row_map, int32_t *src_slot,
+                                  void *X_perm, void *X_fp8, float *X_scale, int32_t *status, void *workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+size_t fused_workspace_bytes(int E);
 
 cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm,
                            void *X_fp8, float *X_scale, int32_t *status, cudaStream_t stream);

@@ -4,28 +4,44 @@
 // section 融合Triton路由内核): logits = tokens @ gate_w, softmax over E,
 // top-K, renorm -- in one pass over X, so the logits never reach HBM.
 //
-// GB300 design (not the page's 64x64 SRAM tiling):
-//   * one CTA per 128-token tile, 6 warps:
-//       warp 0    TMA producer: X tile [128 x 64] and gate-weight slab
-//                 [64 x EP] per K-step, 128-byte swizzle, into a ring of
-//                 `stages` shared-memory slots (mbarrier full/empty pairs);
-//       warp 1    MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> fp32),
-//                 M = 128, N = E rounded up to 16, four K = 16 steps per
-//                 slot; the fp32 logits accumulate in TMEM (128 lanes x N
-//                 columns) and never leave the SM;
-//       warps 2-5 epilogue: each thread owns one token (TMEM lane), reads its
-//                 E logits with tcgen05.ld, adds the bias, keeps the running
-//                 top-K in registers (one pass, K compare-exchange steps per
-//                 candidate -- the same K largest, in the same order and with
-//                 the same tie rule as K rounds of selection), then forms the
-//                 weights with an fp32 softmax.
-//   * X is K-major (row-major [N,H]); the gate weight [H,E] is read as it is
-//     stored, as an MN-major B operand (E contiguous), so no transpose pass.
-//   * Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the CTA
-//     records MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM, exits.
+// GB300 design (not the page's 64x64 SRAM tiling).  One CTA per SM, 10 warps:
+//   warp 0     TMA producer: X tile [128 x 64] and gate-weight slab [64 x EP]
+//              per K-step, 128-byte swizzle, into a ring of `stages` shared
+//              memory slots (full/empty mbarrier pairs), running ahead across
+//              tile boundaries;
+//   warp 1     MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), M = 128,
+//              N = E rounded up to 16, four K = 16 steps per slot, into one of
+//              two TMEM accumulators (128 lanes x N fp32 columns each);
+//   warps 2-9  epilogue: two warps per TMEM lane quarter, each taking half of
+//              the expert columns of its 32 tokens.
+// X is K-major (row-major [N,H]); the gate weight [H,E] is read as stored, as an
+// MN-major B operand (E contiguous), so no transpose pass is needed.
+//
+// Two modes:
+//   * persistent (many tokens): CTA c takes tiles c, c + grid, ...; the
+//     epilogue of tile t overlaps the MMAs of tile t + 1 (double-buffered TMEM).
+//   * split (few tokens: the 128-token tiles alone would leave most SMs idle):
+//     a thread-block cluster of S CTAs shares a tile, CTA r taking 1/S of the
+//     H range; the partial logits go through distributed shared memory to the
+//     CTA that owns those 128/S tokens, which sums the S slices in a fixed order
+//     and finishes its tokens with 2S threads per token.
+// Top-K: each thread keeps sorted top-K lists in registers (a candidate enters
+// with K compare-exchange steps, lists fed with increasing expert ids so equal
+// logits keep the lower id first); the lists of a token are merged by K rounds
+// of "take the best head" -- K-round selection over list heads, through shared
+// memory between the two column halves or warp shuffles between the threads of
+// a token.  Ties go to the lower expert index; NaN counts as -inf.
+//
+// The epilogue is written as rolled loops: it runs once or a few times per CTA,
+// and straight-line unrolled code there is dominated by instruction fetch.
+//
+// Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the CTA records
+// MOE_ERR_TIMEOUT, drains its outstanding copies and MMAs, still reaches the
+// cluster barriers (so no peer waits forever), frees TMEM and exits.
 #include <math.h>
 
 #include <atomic>
+#include <map>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -33,55 +49,200 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;        // tokens per CTA (UMMA M)
-constexpr int kBK = 64;         // bf16 per 128-byte swizzle row (one K-step slot)
-constexpr int kThreads = 192;   // 6 warps
-constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KiB X tile per slot
-constexpr uint32_t kBBoxBytes = kBK * 64 * 2; // 8 KiB per 64-expert gate box
+constexpr int kBM = 128;                       // tokens per tile (UMMA M)
+constexpr int kBK = 64;                        // bf16 per 128-byte swizzle row (one K-step)
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // 320
+constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KiB X tile per slot
+constexpr uint32_t kBBoxBytes = kBK * 64 * 2;  // 8 KiB per 64-expert gate box
+constexpr int kMaxStages = 12;
+constexpr int kEmpty = 0x7fffffff;             // index of an empty list slot
 
 struct TcSmemTail {
-    uint64_t full[8];
-    uint64_t empty[8];
-    uint64_t acc_full;
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 
-__device__ __forceinline__ bool ranks_above(float v, int i, float bv, int bi)
+struct TcParams {
+    const float *bias;
+    int32_t *topk_idx;
+    float *topk_w;
+    int32_t *status;
+    int N, H, E, K, renorm;
+    int EP, NP, stages, nsplit, kb_per, tiles;
+    uint32_t tmem_cols;
+    uint32_t exch_off;  // byte offset of the epilogue exchange area (from the aligned base)
+    uint32_t tail_off;  // byte offset of TcSmemTail
+};
+
+// Row stride (floats) of the split-mode staging buffer: NP + 4 keeps rows
+// 16-byte aligned for vector DSMEM stores and spreads banks.
+__host__ __device__ constexpr int stage_row_floats(int NP) { return NP + 4; }
+
+// Epilogue exchange area: per column half a sorted list per token
+// (KMAX values + KMAX ids), per half and token the running (max, sum-exp),
+// and per token the final K logits.
+__host__ __device__ constexpr uint32_t exch_bytes(int kmax)
 {
-    return v > bv || (v == bv && i < bi);
+    return static_cast<uint32_t>(2 * kBM * kmax * 8 + 2 * kBM * 2 * 4 + kBM * kmax * 4);
+}
+
+// Order-preserving int32 key of a logit: NaN counts as -inf, -0 as +0, and
+// keys compare like the floats.  kKeyEmpty (below the key of -inf) marks an
+// empty list slot.
+constexpr int kKeyEmpty = static_cast<int>(0x80000000u);
+
+__device__ __forceinline__ int order_key(float x)
+{
+    x = isnan(x) ? -INFINITY : x + 0.0f;
+    const int b = __float_as_int(x);
+    return b >= 0 ? b : (b ^ 0x7FFFFFFF);
+}
+
+__device__ __forceinline__ float key_value(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF)); }
+
+// (ka, ia) ranks above (kb, ib): larger logit, or equal logit and lower expert id.
+__device__ __forceinline__ bool ranks_above(int ka, int ia, int kb, int ib)
+{
+    return ka > kb || (ka == kb && ia < ib);
+}
+
+// Insert a candidate into a sorted top-KMAX list (keys descending).  The
+// candidate's id is larger than every id already in the list (candidates
+// arrive in increasing id order), so it goes below all equal keys: slot t
+// takes the candidate where it is the first slot with key < new key, the entry
+// above it where a slot above was already displaced, else keeps its own.
+// Every slot decides from the old list alone: no branches, no carried chain.
+template <int KMAX>
+__device__ __forceinline__ void topk_push(int (&k)[KMAX], int (&ix)[KMAX], int nk, int ne)
+{
+    bool prev = false;
+    int pk = kKeyEmpty, pi = kEmpty;
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+        const bool c = nk > k[t];
+        const int ok = k[t], oi = ix[t];
+        k[t] = c ? (prev ? pk : nk) : ok;
+        ix[t] = c ? (prev ? pi : ne) : oi;
+        prev = c;
+        pk = ok;
+        pi = oi;
+    }
 }
 
 template <int KMAX>
-__global__ void __launch_bounds__(kThreads, 2) route_tc_kernel(
-    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-    const float *__restrict__ bias, int N, int H, int E, int K, int renorm, int EP, int NP, int stages,
-    uint32_t tmem_cols, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *status)
+__device__ __forceinline__ void topk_clear(int (&k)[KMAX], int (&ix)[KMAX])
+{
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+        k[t] = kKeyEmpty;
+        ix[t] = kEmpty;
+    }
+}
+
+// Drop the head of a sorted list (shift up by one).
+template <int KMAX>
+__device__ __forceinline__ void topk_pop_if(int (&k)[KMAX], int (&ix)[KMAX], bool pop)
+{
+#pragma unroll
+    for (int t = 0; t + 1 < KMAX; ++t) {
+        k[t] = pop ? k[t + 1] : k[t];
+        ix[t] = pop ? ix[t + 1] : ix[t];
+    }
+    k[KMAX - 1] = pop ? kKeyEmpty : k[KMAX - 1];
+    ix[KMAX - 1] = pop ? kEmpty : ix[KMAX - 1];
+}
+
+__device__ __forceinline__ float logit_of(float acc, float bias)
+{
+    const float x = acc + bias;
+    return isnan(x) ? -INFINITY : x;
+}
+
+// Online max / sum of exp over the logits a thread sees (renorm off only).
+__device__ __forceinline__ void online_sumexp(float x, float &r, float &z)
+{
+    if (x == -INFINITY) return;
+    if (x > r) {
+        z = z * expf(r - x) + 1.f;
+        r = x;
+    } else {
+        z += expf(x - r);
+    }
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t cta)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(cta));
+    return r;
+}
+
+__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+template <int KMAX, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                               const __grid_constant__ CUtensorMap tmW,
+                                                               const TcParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t b_slot_bytes = static_cast<uint32_t>(EP) * kBK * 2;
+    const uint32_t b_slot_bytes = static_cast<uint32_t>(p.EP) * kBK * 2;
     unsigned char *a_base = smem;
-    unsigned char *b_base = smem + static_cast<size_t>(stages) * kABytes;
-    TcSmemTail &tail =
-        *reinterpret_cast<TcSmemTail *>(b_base + static_cast<size_t>(stages) * b_slot_bytes);
+    unsigned char *b_base = smem + static_cast<size_t>(p.stages) * kABytes;
+    TcSmemTail &tail = *reinterpret_cast<TcSmemTail *>(smem + p.tail_off);
     float *bias_s = reinterpret_cast<float *>(&tail + 1);
+    // exchange area, token-minor so that the lanes of a warp touch consecutive words
+    int *lst_k = reinterpret_cast<int *>(smem + p.exch_off);            // [2 halves][KMAX][128] keys
+    int *lst_i = lst_k + 2 * kBM * KMAX;                                   // [2 halves][KMAX][128] ids
+    float *lst_rz = reinterpret_cast<float *>(lst_i + 2 * kBM * KMAX);     // [2 halves][2][128]
+    float *win_v = lst_rz + 2 * kBM * 2;                                   // [KMAX][128]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kBM;
-    const int nk = (H + kBK - 1) / kBK;
+    const uint32_t rank = SPLIT ? cluster_rank() : 0u;
+    const int nk = (p.H + kBK - 1) / kBK;
+    const int kb0 = SPLIT ? static_cast<int>(rank) * p.kb_per : 0;
+    const int kb1 = SPLIT ? min(nk, kb0 + p.kb_per) : nk;
+    const int nkb = kb1 > kb0 ? kb1 - kb0 : 0;    // K-steps of this CTA per tile (0: contributes nothing)
+    const int first_tile = SPLIT ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
+    const int tile_step = SPLIT ? p.tiles : static_cast<int>(gridDim.x);  // split: exactly one tile
+    const int K = p.K;
+    const int E = p.E;
     volatile int *abort_flag = &tail.abort;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < p.stages; ++s) {
             mbar_init(&tail.full[s], 1);
             mbar_init(&tail.empty[s], 1);
         }
-        mbar_init(&tail.acc_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tail.acc_full[b], 1);
+            mbar_init(&tail.acc_empty[b], kEpiWarps);
+        }
         mbar_init(&tail.drain, 1);
         tail.abort = 0;
         fence_mbarrier_init();
@@ -91,151 +252,297 @@ __global__ void __launch_bounds__(kThreads, 2) route_tc_kernel(
         tma_prefetch_desc(&tmW);
     }
     if (warp == 1) {
-        tmem_alloc(&tail.tmem_base, tmem_cols);
+        tmem_alloc(&tail.tmem_base, p.tmem_cols);
         tmem_relinquish();
     }
     // inputs may come from the previous kernel in the stream (programmatic launch)
     pdl_wait_prior_grids();
-    for (int e = threadIdx.x; e < EP; e += kThreads) bias_s[e] = (bias != nullptr && e < E) ? bias[e] : 0.f;
+    for (int e = threadIdx.x; e < p.EP; e += kThreads) bias_s[e] = (p.bias != nullptr && e < E) ? p.bias[e] : 0.f;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = tail.tmem_base;
 
+    bool acc_ok = false;  // split mode, epilogue threads: the partial accumulator is complete
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol_x = l2_policy_evict_first();
             const uint64_t pol_w = l2_policy_evict_last();
-            int issued = 0;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % stages;
-                const uint32_t use = static_cast<uint32_t>(kb / stages);
-                if (!mbar_wait_bounded(&tail.empty[s], (use & 1u) ^ 1u, abort_flag)) break;
-                mbar_arrive_expect_tx(&tail.full[s], kABytes + b_slot_bytes);
-                tma_load_2d(a_base + static_cast<size_t>(s) * kABytes, &tmX, &tail.full[s], kb * kBK, m0, pol_x);
-                for (int j = 0; j < EP / 64; ++j)
-                    tma_load_2d(b_base + static_cast<size_t>(s) * b_slot_bytes + j * kBBoxBytes, &tmW,
-                                &tail.full[s], j * 64, kb * kBK, pol_w);
-                issued = kb + 1;
+            uint32_t g = 0;  // K-steps issued so far (across tiles)
+            bool stop = false;
+            for (int tile = first_tile; tile < p.tiles && !stop; tile += tile_step) {
+                const int m0 = tile * kBM;
+                for (int i = 0; i < nkb; ++i) {
+                    const uint32_t s = g % p.stages;
+                    const uint32_t use = g / p.stages;
+                    if (!mbar_wait_bounded(&tail.empty[s], (use & 1u) ^ 1u, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    const int kb = kb0 + i;
+                    mbar_arrive_expect_tx(&tail.full[s], kABytes + b_slot_bytes);
+                    tma_load_2d(a_base + static_cast<size_t>(s) * kABytes, &tmX, &tail.full[s], kb * kBK, m0, pol_x);
+                    for (int j = 0; j < p.EP / 64; ++j)
+                        tma_load_2d(b_base + static_cast<size_t>(s) * b_slot_bytes + j * kBBoxBytes, &tmW,
+                                    &tail.full[s], j * 64, kb * kBK, pol_w);
+                    ++g;
+                }
             }
             if (*abort_flag) {
-                // let the copies already issued land before the CTA exits
-                for (int kb = issued - stages < 0 ? 0 : issued - stages; kb < issued; ++kb) {
+                // let the copies already issued land before the shared memory is reused
+                const uint32_t from = g > static_cast<uint32_t>(p.stages) ? g - p.stages : 0u;
+                for (uint32_t x = from; x < g; ++x) {
                     volatile int no_abort = 0;
-                    mbar_wait_bounded(&tail.full[kb % stages], static_cast<uint32_t>(kb / stages) & 1u,
-                                      &no_abort);
+                    mbar_wait_bounded(&tail.full[x % p.stages], (x / p.stages) & 1u, &no_abort);
                 }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = make_idesc_bf16_f32(kBM, static_cast<uint32_t>(NP), 0u, 1u);
+            const uint32_t idesc = make_idesc_bf16_f32(kBM, static_cast<uint32_t>(p.NP), 0u, 1u);
             const uint32_t a0 = smem_u32(a_base);
             const uint32_t b0 = smem_u32(b_base);
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % stages;
-                const uint32_t use = static_cast<uint32_t>(kb / stages);
-                if (!mbar_wait_bounded(&tail.full[s], use & 1u, abort_flag)) break;
+            uint32_t g = 0;
+            int j = 0;
+            bool stop = false;
+            for (int tile = first_tile; tile < p.tiles; tile += tile_step, ++j) {
+                const int b = j & 1;
+                if (!mbar_wait_bounded(&tail.acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag)) break;
                 tc_fence_after_sync();
-                const uint32_t a_s = a0 + static_cast<uint32_t>(s) * kABytes;
-                const uint32_t b_s = b0 + static_cast<uint32_t>(s) * b_slot_bytes;
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.NP);
+                for (int i = 0; i < nkb; ++i) {
+                    const uint32_t s = g % p.stages;
+                    const uint32_t use = g / p.stages;
+                    if (!mbar_wait_bounded(&tail.full[s], use & 1u, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_s = a0 + s * kABytes;
+                    const uint32_t b_s = b0 + s * b_slot_bytes;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    // A: K-major, 128-byte rows, 8-row groups 1024 B apart; +32 B per K=16 step
-                    const uint64_t a_desc = make_smem_desc_sw128(a_s + kk * 32, 16, 1024);
-                    // B: MN-major, 64-expert atoms 8 KiB apart (LBO), 8-row K groups 1024 B
-                    // apart (SBO); +16 rows x 128 B per K=16 step
-                    const uint64_t b_desc = make_smem_desc_sw128(b_s + kk * 2048, kBBoxBytes, 1024);
-                    tc_mma_f16(tmem_base, a_desc, b_desc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // A: K-major, 128-byte rows, 8-row groups 1024 B apart; +32 B per K=16 step
+                        const uint64_t a_desc = make_smem_desc_sw128(a_s + kk * 32, 16, 1024);
+                        // B: MN-major, 64-expert atoms 8 KiB apart (LBO), 8-row K groups 1024 B
+                        // apart (SBO); +16 rows x 128 B per K=16 step
+                        const uint64_t b_desc = make_smem_desc_sw128(b_s + kk * 2048, kBBoxBytes, 1024);
+                        tc_mma_f16(d_tmem, a_desc, b_desc, idesc, (i | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(&tail.empty[s]);  // slot free once these MMAs have read it
+                    ++g;
                 }
-                tc_commit(&tail.empty[s]);  // slot free once these MMAs have read it
+                if (stop) break;
+                tc_commit(&tail.acc_full[b]);   // this tile's logits (or partial logits) complete
             }
-            tc_commit(&tail.acc_full);      // logits complete
             tc_commit(&tail.drain);
             volatile int no_abort = 0;
             mbar_wait_bounded(&tail.drain, 0, &no_abort);
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int n = m0 + q * 32 + lane;
-        if (mbar_wait_bounded(&tail.acc_full, 0, abort_flag)) {
-            tc_fence_after_sync();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-            float bv[KMAX];
-            int bi[KMAX];
+        // ------------------------------------------------------------ epilogue warps
+        const int q = warp & 3;                // TMEM lane quarter this warp may access
+        const int h = (warp - 2) >> 2;         // which half of the expert columns
+        const int row = q * 32 + lane;         // token row of the tile (= TMEM lane)
+        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const int nph = p.NP >> 1;             // columns per half (a multiple of 8)
+        if constexpr (!SPLIT) {
+            int j = 0;
+            for (int tile = first_tile; tile < p.tiles; tile += tile_step, ++j) {
+                const int b = j & 1;
+                if (!mbar_wait_bounded(&tail.acc_full[b], (j >> 1) & 1, abort_flag, 64)) break;
+                tc_fence_after_sync();
+                // ---- this half's columns: two interleaved lists for ILP
+                int ak[KMAX], bk[KMAX], ai[KMAX], bi[KMAX];
+                topk_clear<KMAX>(ak, ai);
+                topk_clear<KMAX>(bk, bi);
+                float r = -INFINITY, z = 0.f;
+                const int c_end = min(E, h * nph + nph);
+                const uint32_t col_addr = lane_addr + static_cast<uint32_t>(b * p.NP);
+#pragma unroll 1
+                for (int c = h * nph; c < c_end; c += 8) {
+                    float v[8];
+                    tmem_ld_32x32b_x8(col_addr + c, v);
+                    tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                bv[j] = -INFINITY;
-                bi[j] = 0x7fffffff;
-            }
-            for (int c0 = 0; c0 < NP; c0 += 32) {
-                float v[32];
-                tmem_ld_32x32b_x32(taddr + c0, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int e = c0 + j;
-                    if (e >= E) break;
-                    float x = v[j] + bias_s[e];
-                    if (isnan(x)) x = -INFINITY;
-                    if (ranks_above(x, e, bv[KMAX - 1], bi[KMAX - 1])) {
-                        float cv = x;
-                        int ci = e;
-#pragma unroll
-                        for (int t = 0; t < KMAX; ++t) {
-                            const bool up = ranks_above(cv, ci, bv[t], bi[t]);
-                            const float ov = bv[t];
-                            const int oi = bi[t];
-                            bv[t] = up ? cv : ov;
-                            bi[t] = up ? ci : oi;
-                            cv = up ? ov : cv;
-                            ci = up ? oi : ci;
+                    for (int t = 0; t < 8; t += 2) {
+                        const float x0 = logit_of(v[t], bias_s[c + t]);
+                        const float x1 = logit_of(v[t + 1], bias_s[c + t + 1]);
+                        topk_push<KMAX>(ak, ai, order_key(x0), c + t);
+                        topk_push<KMAX>(bk, bi, order_key(x1), c + t + 1);
+                        if (!p.renorm) {
+                            online_sumexp(x0, r, z);
+                            online_sumexp(x1, r, z);
                         }
                     }
                 }
-            }
-            const float m = bv[0];
-            float denom = 0.f;
-            if (renorm) {
-#pragma unroll
-                for (int t = 0; t < KMAX; ++t)
-                    if (t < K) denom += expf(bv[t] - m);
-            } else {
-                for (int c0 = 0; c0 < NP; c0 += 32) {
-                    float v[32];
-                    tmem_ld_32x32b_x32(taddr + c0, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int e = c0 + j;
-                        if (e >= E) break;
-                        const float x = v[j] + bias_s[e];
-                        if (!isnan(x)) denom += expf(x - m);
+                // the accumulator may be overwritten by the next tile's MMAs from here on
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tail.acc_empty[b]);
+                // ---- merge the two lists into this half's sorted top-K (shared memory)
+                int *my_k = lst_k + h * KMAX * kBM + row;
+                int *my_i = lst_i + h * KMAX * kBM + row;
+#pragma unroll 1
+                for (int k = 0; k < K; ++k) {
+                    const bool take_b = ranks_above(bk[0], bi[0], ak[0], ai[0]);
+                    my_k[k * kBM] = take_b ? bk[0] : ak[0];
+                    my_i[k * kBM] = take_b ? bi[0] : ai[0];
+                    topk_pop_if<KMAX>(ak, ai, !take_b);
+                    topk_pop_if<KMAX>(bk, bi, take_b);
+                }
+                lst_rz[(h * 2) * kBM + row] = r;
+                lst_rz[(h * 2 + 1) * kBM + row] = z;
+                named_barrier_sync(1 + q, 64);   // both halves' lists are ready
+                if (h == 0) {
+                    // ---- two-way merge of the halves, K rounds; ids written as selected
+                    const int n = tile * kBM + row;
+                    const int *ok = lst_k + KMAX * kBM + row;
+                    const int *oi = lst_i + KMAX * kBM + row;
+                    float *wrow = win_v + row;
+                    int pa = 0, pb = 0;
+#pragma unroll 1
+                    for (int k = 0; k < K; ++k) {
+                        const int ka = pa < K ? my_k[pa * kBM] : kKeyEmpty;
+                        const int ia = pa < K ? my_i[pa * kBM] : kEmpty;
+                        const int kb = pb < K ? ok[pb * kBM] : kKeyEmpty;
+                        const int ib = pb < K ? oi[pb * kBM] : kEmpty;
+                        const bool take_b = ranks_above(kb, ib, ka, ia);
+                        wrow[k * kBM] = key_value(take_b ? kb : ka);
+                        if (n < p.N) p.topk_idx[static_cast<int64_t>(n) * K + k] = take_b ? ib : ia;
+                        pa += take_b ? 0 : 1;
+                        pb += take_b ? 1 : 0;
+                    }
+                    const float m = wrow[0];
+                    float denom = 0.f;
+                    if (p.renorm) {
+#pragma unroll 1
+                        for (int k = 0; k < K; ++k) denom += expf(wrow[k * kBM] - m);
+                    } else {
+                        const float r0 = lst_rz[row], z0 = lst_rz[kBM + row];
+                        const float r1 = lst_rz[2 * kBM + row], z1 = lst_rz[3 * kBM + row];
+                        denom = (z0 > 0.f ? z0 * expf(r0 - m) : 0.f) + (z1 > 0.f ? z1 * expf(r1 - m) : 0.f);
+                    }
+                    if (n < p.N) {
+#pragma unroll 1
+                        for (int k = 0; k < K; ++k)
+                            p.topk_w[static_cast<int64_t>(n) * K + k] = expf(wrow[k * kBM] - m) / denom;
                     }
                 }
+                named_barrier_sync(1 + q, 64);   // the lists have been consumed
             }
-            if (n < N) {
-#pragma unroll
-                for (int t = 0; t < KMAX; ++t) {
-                    if (t < K) {
-                        topk_idx[static_cast<int64_t>(n) * K + t] = bi[t];
-                        topk_w[static_cast<int64_t>(n) * K + t] = expf(bv[t] - m) / denom;
-                    }
-                }
+        } else {
+            acc_ok = mbar_wait_bounded(&tail.acc_full[0], 0, abort_flag, 64);
+            tc_fence_after_sync();
+        }
+    }
+
+    if constexpr (SPLIT) {
+        // ------------------------------------------------------------ split-K reduction through DSMEM
+        const int S = p.nsplit;
+        const int R = kBM / S;                          // tokens owned by each CTA of the cluster
+        const int RS = stage_row_floats(p.NP);
+        float *buf = reinterpret_cast<float *>(smem);   // [S slices][R rows][RS], reuses the ring
+        __syncwarp();
+        cluster_sync_all();                             // #1: every CTA's ring is free
+        if (warp >= 2 && acc_ok && nkb > 0) {
+            const int q = warp & 3;
+            const int h = (warp - 2) >> 2;
+            const int row = q * 32 + lane;
+            const int nph = p.NP >> 1;
+            const uint32_t owner = static_cast<uint32_t>(row / R);
+            const uint32_t local = smem_u32(buf + (static_cast<int>(rank) * R + row % R) * RS);
+            const uint32_t remote = dsmem_map(local, owner);
+            const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+            for (int c = h * nph; c < h * nph + nph; c += 8) {
+                float v[8];
+                tmem_ld_32x32b_x8(lane_addr + c, v);
+                tmem_ld_wait();
+                st_dsmem_v4(remote + c * 4, v[0], v[1], v[2], v[3]);
+                st_dsmem_v4(remote + c * 4 + 16, v[4], v[5], v[6], v[7]);
             }
         }
         tc_fence_before_sync();
+        __syncwarp();
+        cluster_sync_all();                             // #2: all partial logits delivered
+        if (warp >= 2) {
+            const int t = threadIdx.x - 64;             // 0..255
+            const int G = (32 * kEpiWarps) / R;         // threads per token: 2S (4, 8 or 16)
+            const int lrow = t / G;
+            const int part = t % G;
+            const int n = first_tile * kBM + static_cast<int>(rank) * R + lrow;
+            const int nslices = min(S, (nk + p.kb_per - 1) / p.kb_per);  // CTAs that had K-steps
+            int bk[KMAX], bi[KMAX];
+            topk_clear<KMAX>(bk, bi);
+            const float *rowbuf = buf + lrow * RS;
+#pragma unroll 1
+            for (int col = part; col < E; col += G) {
+                float x = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)   // independent loads, summed in slice order
+                    if (c < nslices) x += rowbuf[c * R * RS + col];
+                topk_push<KMAX>(bk, bi, order_key(logit_of(x, bias_s[col])), col);
+            }
+            // K rounds of selection across the G threads of the token (warp shuffles)
+            float *wrow = win_v + lrow;
+            float m = 0.f;
+#pragma unroll 1
+            for (int k = 0; k < K; ++k) {
+                int v = bk[0];
+                int i = bi[0];
+#pragma unroll 1
+                for (int o = G >> 1; o > 0; o >>= 1) {
+                    const int ov = __shfl_xor_sync(0xffffffffu, v, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+                    const bool up = ranks_above(ov, oi, v, i);
+                    v = up ? ov : v;
+                    i = up ? oi : i;
+                }
+                const float fv = key_value(v);
+                if (k == 0) m = fv;
+                topk_pop_if<KMAX>(bk, bi, bi[0] == i);
+                if (part == 0) {
+                    wrow[k * kBM] = fv;
+                    if (n < p.N) p.topk_idx[static_cast<int64_t>(n) * K + k] = i;
+                }
+            }
+            float z = 0.f;
+            if (!p.renorm) {
+#pragma unroll 1
+                for (int col = part; col < E; col += G) {
+                    float x = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        if (c < nslices) x += rowbuf[c * R * RS + col];
+                    x = logit_of(x, bias_s[col]);
+                    if (x != -INFINITY) z += expf(x - m);
+                }
+#pragma unroll 1
+                for (int o = G >> 1; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            }
+            if (part == 0 && n < p.N) {
+                float denom = z;
+                if (p.renorm) {
+                    denom = 0.f;
+#pragma unroll 1
+                    for (int k = 0; k < K; ++k) denom += expf(wrow[k * kBM] - m);
+                }
+#pragma unroll 1
+                for (int k = 0; k < K; ++k)
+                    p.topk_w[static_cast<int64_t>(n) * K + k] = expf(wrow[k * kBM] - m) / denom;
+            }
+        }
     }
 
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, tmem_cols);
+        tmem_dealloc(tmem_base, p.tmem_cols);
     }
-    if (threadIdx.x == 0 && tail.abort) report_status(status, MOE_ERR_TIMEOUT);
+    if (threadIdx.x == 0 && tail.abort) report_status(p.status, MOE_ERR_TIMEOUT);
     pdl_launch_dependents();
 }
 
@@ -251,12 +558,12 @@ EncodeTiledFn encode_tiled_fn()
     static std::once_flag once;
     static EncodeTiledFn fn = nullptr;
     std::call_once(once, [] {
-        void *p = nullptr;
+        void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
     });
     return fn;
 }
@@ -275,55 +582,150 @@ bool encode_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct TcPlan {
-    int EP, NP, stages;
-    uint32_t tmem_cols;
+int kmax_for(int K) { return K <= 2 ? 2 : K <= 4 ? 4 : K <= 8 ? 8 : 16; }
+
+constexpr size_t kSmemLimit = 227 * 1024;
+
+// Layout of a launch's shared memory: 1 KiB alignment slack, the TMA ring (or,
+// if larger, the split staging area), the exchange area, the tail and the bias.
+struct TcLayout {
+    int stages;
+    uint32_t exch_off, tail_off;
     size_t smem;
 };
 
-TcPlan plan_for(int E)
+bool layout_for(int EP, int NP, int kmax, bool split, TcLayout &L)
 {
-    TcPlan p;
-    p.EP = (E + 63) / 64 * 64;
-    p.NP = (E + 15) / 16 * 16;
-    const uint32_t slot = kABytes + static_cast<uint32_t>(p.EP) * kBK * 2;
-    // two CTAs per SM while that still leaves >= 2 slots (~100 KiB each)
-    int st = static_cast<int>((100u * 1024u) / slot);
-    if (st > 8) st = 8;
-    if (st < 2) st = 2;
-    p.stages = st;
-    uint32_t cols = 32;
-    while (cols < static_cast<uint32_t>(p.NP)) cols <<= 1;
-    p.tmem_cols = cols;
-    p.smem = 1024 + static_cast<size_t>(st) * slot + sizeof(TcSmemTail) + sizeof(float) * p.EP;
-    return p;
+    const size_t slot = kABytes + static_cast<size_t>(EP) * kBK * 2;
+    const size_t staging = split ? static_cast<size_t>(kBM) * stage_row_floats(NP) * sizeof(float) : 0;
+    const size_t fixed = 1024 + exch_bytes(kmax) + sizeof(TcSmemTail) + sizeof(float) * EP;
+    for (int st = kMaxStages; st >= 2; --st) {
+        size_t area = static_cast<size_t>(st) * slot;
+        if (staging > area) area = staging;
+        area = (area + 1023) & ~size_t(1023);
+        if (fixed + area <= kSmemLimit) {
+            L.stages = st;
+            L.exch_off = static_cast<uint32_t>(area);
+            L.tail_off = static_cast<uint32_t>(area + exch_bytes(kmax));
+            L.smem = fixed + area;
+            return true;
+        }
+    }
+    return false;
 }
 
-template <int KMAX>
-cudaError_t launch_tc_k(const RouteArgs &a, const TcPlan &p, const CUtensorMap &tmX, const CUtensorMap &tmW,
-                        cudaStream_t stream, int dev)
+template <int KMAX, bool SPLIT>
+cudaError_t set_smem_attr(int dev)
 {
     static std::atomic<uint64_t> configured{0};
     const uint64_t bit = 1ull << (dev & 63);
-    cudaError_t err;
-    if (!(configured.load() & bit)) {
-        err = cudaFuncSetAttribute(route_tc_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   227 * 1024);
-        if (err != cudaSuccess) return err;
-        configured.fetch_or(bit);
+    if (configured.load() & bit) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(route_tc_kernel<KMAX, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kSmemLimit));
+    if (err == cudaSuccess) configured.fetch_or(bit);
+    return err;
+}
+
+template <int KMAX>
+int max_active_clusters(size_t smem, int S, int dev)
+{
+    // cached per (device, cluster size, shared memory size)
+    static std::mutex mu;
+    static std::map<uint64_t, int> cache;
+    const uint64_t key = (static_cast<uint64_t>(dev) << 40) | (static_cast<uint64_t>(S) << 32) | smem;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(static_cast<unsigned>((a.N + kBM - 1) / kBM), 1, 1);
+    cfg.gridDim = dim3(S, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = stream;
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.dynamicSmemBytes = smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX>, tmX, tmW, a.bias, static_cast<int>(a.N), a.H, a.E, a.K,
-                              a.renorm, p.EP, p.NP, p.stages, p.tmem_cols, a.topk_idx, a.topk_w, a.status);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, route_tc_kernel<KMAX, true>, &cfg) != cudaSuccess) n = 0;
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = n;
+    return n;
+}
+
+template <int KMAX>
+cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CUtensorMap &tmW, cudaStream_t stream,
+                            int dev)
+{
+    const int sms = device_sm_count(dev);
+    TcParams q;
+    q.bias = a.bias;
+    q.topk_idx = a.topk_idx;
+    q.topk_w = a.topk_w;
+    q.status = a.status;
+    q.N = static_cast<int>(a.N);
+    q.H = a.H;
+    q.E = a.E;
+    q.K = a.K;
+    q.renorm = a.renorm;
+    q.EP = (a.E + 63) / 64 * 64;
+    q.NP = (a.E + 15) / 16 * 16;
+    q.tiles = static_cast<int>((a.N + kBM - 1) / kBM);
+    const int nk = (a.H + kBK - 1) / kBK;
+
+    // split H over a cluster while the tiles alone leave SMs idle (one CTA per SM)
+    int S = 1;
+    while (S < 8 && static_cast<int64_t>(q.tiles) * S * 2 <= sms && nk >= 2 * S) S *= 2;
+
+    cudaError_t err;
+    TcLayout L;
+    if (S > 1) {
+        if ((err = set_smem_attr<KMAX, true>(dev)) != cudaSuccess) return err;
+        // every cluster must be resident at once (one wave), else use a smaller split
+        for (; S > 1; S >>= 1) {
+            if (!layout_for(q.EP, q.NP, KMAX, true, L)) continue;
+            if (max_active_clusters<KMAX>(L.smem, S, dev) >= q.tiles) break;
+        }
+    }
+    const bool split = S > 1;
+    if (!layout_for(q.EP, q.NP, KMAX, split, L)) return cudaErrorInvalidConfiguration;
+    q.stages = L.stages;
+    q.exch_off = L.exch_off;
+    q.tail_off = L.tail_off;
+    q.nsplit = S;
+    q.kb_per = (nk + S - 1) / S;
+    uint32_t cols = 32;
+    const uint32_t need = static_cast<uint32_t>(split ? q.NP : 2 * q.NP);  // persistent: two accumulators
+    while (cols < need) cols <<= 1;
+    q.tmem_cols = cols;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (split) {
+        cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(q.tiles), 1);
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = S;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    } else {
+        cfg.gridDim = dim3(static_cast<unsigned>(q.tiles < sms ? q.tiles : sms), 1, 1);
+    }
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    if (split) return cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, true>, tmX, tmW, q);
+    if ((err = set_smem_attr<KMAX, false>(dev)) != cudaSuccess) return err;
+    return cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, false>, tmX, tmW, q);
 }
 
 }  // namespace
@@ -343,16 +745,17 @@ cudaError_t launch_route_tc(const RouteArgs &a, cudaStream_t stream)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const TcPlan p = plan_for(a.E);
     CUtensorMap tmX, tmW;
     if (!encode_2d_bf16(&tmX, a.X, static_cast<uint64_t>(a.H), static_cast<uint64_t>(a.N), kBK, kBM))
         return cudaErrorInvalidValue;
     if (!encode_2d_bf16(&tmW, a.W, static_cast<uint64_t>(a.E), static_cast<uint64_t>(a.H), 64, kBK))
         return cudaErrorInvalidValue;
-    if (a.K <= 2) return launch_tc_k<2>(a, p, tmX, tmW, stream, dev);
-    if (a.K <= 4) return launch_tc_k<4>(a, p, tmX, tmW, stream, dev);
-    if (a.K <= 8) return launch_tc_k<8>(a, p, tmX, tmW, stream, dev);
-    return launch_tc_k<16>(a, p, tmX, tmW, stream, dev);
+    switch (kmax_for(a.K)) {
+    case 2: return plan_and_launch<2>(a, tmX, tmW, stream, dev);
+    case 4: return plan_and_launch<4>(a, tmX, tmW, stream, dev);
+    case 8: return plan_and_launch<8>(a, tmX, tmW, stream, dev);
+    default: return plan_and_launch<16>(a, tmX, tmW, stream, dev);
+    }
 }
 
 }  // namespace moe

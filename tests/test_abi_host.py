@@ -83,7 +83,11 @@ def dispatch(L, idx=A, X=None, N=16, H=64, E=16, K=2, counts=A2, offsets=A3, row
 
 
 def test_dispatch_validation(L):
-    assert L.moe_dispatch_workspace_size(1 << 20, 64, 8) == 0
+    assert L.moe_dispatch_workspace_size(1 << 20, 64, 8) >= 256 + 64 * 4
+    ws = L.moe_dispatch_workspace_size(16, 16, 2)
+    assert dispatch(L, ws=A, ws_bytes=ws - 4) == WORKSPACE                 # too small
+    assert dispatch(L, ws=None, ws_bytes=ws) == WORKSPACE                  # size without a buffer
+    assert dispatch(L, ws=A + 16, ws_bytes=ws) == MISALIGNED               # 256-byte alignment
     assert dispatch(L, E=0) == INVALID
     assert dispatch(L, K=0) == INVALID
     assert dispatch(L, counts=None) == INVALID

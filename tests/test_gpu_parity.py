@@ -60,7 +60,7 @@ def gpu_fixture(Xp, counts, E):
 
 TC_SHAPES = [(1, 8, 8, 1), (7, 64, 16, 2), (129, 256, 16, 2), (300, 1024, 64, 4), (257, 512, 128, 8),
              (130, 2048, 256, 16), (65, 96, 48, 3), (33, 40, 24, 5), (200, 128, 8, 8), (513, 320, 32, 2),
-             (1000, 4096, 64, 2)]
+             (1000, 4096, 64, 2), (20000, 128, 256, 16), (40000, 256, 64, 2), (25000, 512, 128, 8)]
 SIMT_ONLY_SHAPES = [(50, 64, 2, 2), (70, 128, 7, 3), (40, 256, 255, 8), (17, 24, 1, 1), (90, 512, 100, 6)]
 
 
@@ -139,11 +139,12 @@ DISPATCH_CASES = [(1, 1, 1), (7, 4, 2), (513, 16, 2), (4096, 64, 4), (20000, 128
                   (1000, 256, 16), (10, 256, 2), (70000, 64, 2)]
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("N,E,K", DISPATCH_CASES)
-def test_dispatch_matches_oracle(N, E, K):
+def test_dispatch_matches_oracle(N, E, K, fused):
     idx = mi.random_topk_idx(N, E, K, seed=N + E + K)
     st = status_word()
-    d = moe.dispatch(idx.to(DEV), E, status=st)
+    d = moe.dispatch(idx.to(DEV), E, fused=fused, status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
     c, o, r, s = oracle.dispatch(idx.numpy(), E)
@@ -154,12 +155,13 @@ def test_dispatch_matches_oracle(N, E, K):
     assert int(d.expert_counts.sum()) == N * K
 
 
-def test_dispatch_hot_experts():
+@pytest.mark.parametrize("fused", [True, False])
+def test_dispatch_hot_experts(fused):
     # every token picks experts 0..K-1: maximal skew, most experts empty
     N, E, K = 50000, 64, 2
     idx = torch.arange(K, dtype=torch.int32).repeat(N, 1).contiguous()
     idx[::2] = idx[::2].flip(1)
-    d = moe.dispatch(idx.to(DEV), E)
+    d = moe.dispatch(idx.to(DEV), E, fused=fused)
     c, o, r, s = oracle.dispatch(idx.numpy(), E)
     assert np.array_equal(d.row_map.cpu().numpy(), r)
     assert np.array_equal(d.expert_offsets.cpu().numpy(), o)
@@ -172,12 +174,13 @@ def test_dispatch_empty_writes_zero_counts():
     assert int(d.expert_counts.abs().sum()) == 0 and int(d.expert_offsets.abs().sum()) == 0
 
 
-def test_dispatch_bad_index_reports_status():
+@pytest.mark.parametrize("fused", [True, False])
+def test_dispatch_bad_index_reports_status(fused):
     idx = mi.random_topk_idx(100, 8, 2, seed=1)
     idx[5, 1] = 8
     idx[77, 0] = -3
     st = status_word()
-    moe.dispatch(idx.to(DEV), 8, status=st)
+    moe.dispatch(idx.to(DEV), 8, fused=fused, status=st)
     torch.cuda.synchronize()
     assert st.item() == moe.ERR_BAD_INDEX
 
@@ -210,6 +213,42 @@ def test_permute_matches_oracle(N, H, K, fp8):
     else:
         rXp = ref
     assert np.array_equal(bits(Xp), rXp)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("N,H,E,K,fp8,bf16", [(513, 1024, 16, 2, False, True), (300, 2048, 64, 8, True, True),
+                                              (257, 384, 32, 3, True, False), (1, 8, 4, 1, False, True),
+                                              (20000, 256, 128, 8, True, True)])
+def test_dispatch_with_rows_matches_oracle(N, H, E, K, fp8, bf16, fused):
+    X = mi.random_bf16((N, H), seed=N + H + K, scale=2.0)
+    idx = mi.random_topk_idx(N, E, K, seed=N + E)
+    st = status_word()
+    d = moe.dispatch(idx.to(DEV), E, X.to(DEV), fp8=fp8, bf16=bf16, fused=fused, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    c, o, r, s = oracle.dispatch(idx.numpy(), E)
+    assert np.array_equal(d.row_map.cpu().numpy(), r) and np.array_equal(d.expert_offsets.cpu().numpy(), o)
+    ref = oracle.permute(bits(X), r, K, fp8=fp8)
+    rXp = ref[0] if fp8 else ref
+    if bf16:
+        assert np.array_equal(bits(d.X_perm), rXp)
+    if fp8:
+        assert np.array_equal(d.X_fp8.cpu().numpy(), ref[1])
+        assert np.array_equal(d.X_scale.cpu().numpy(), ref[2])
+
+
+def test_dispatch_workspace_reused_many_times():
+    # the barrier counters must return to zero after every call
+    E = 64
+    ws = torch.zeros(moe.dispatch_workspace_size(0, E, 1), dtype=torch.uint8, device=DEV)
+    for seed in range(30):
+        N = 100 + 997 * seed
+        idx = mi.random_topk_idx(N, E, 2, seed=seed)
+        d = moe.dispatch(idx.to(DEV), E, workspace=ws)
+        c, o, r, s = oracle.dispatch(idx.numpy(), E)
+        assert np.array_equal(d.row_map.cpu().numpy(), r)
+    torch.cuda.synchronize()
+    assert int(ws[:8].abs().sum()) == 0
 
 
 def test_permute_fp8_only():
