@@ -274,7 +274,10 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     assert st.item() == 0, moe.status_string(st.item())
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # ---- timed region: K whole steps, each bracketed by an event pair (the L2
+    # flush in between is outside the brackets; no events between the kernels
+    # of a step, so consecutive launches may overlap their prologues)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -285,23 +288,15 @@ def run_ours(args, rank, world, local):
     t0 = time.time()
     for i in range(args.steps):
         flush.zero_()
-        step(evs[i])
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
     t1 = time.time()
-    if sampler:
-        time.sleep(0.2)
-        sampler.stop()
     assert st.item() == 0, moe.status_string(st.item())
-
-    names = ["route", "dispatch", "combine"]
-    per = {n: [] for n in names}
-    step_ms = []
-    for ev in evs:
-        for j, n in enumerate(names):
-            per[n].append(ev[j].elapsed_time(ev[j + 1]))
-        step_ms.append(ev[0].elapsed_time(ev[3]))
+    step_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
     total_ms = sum(step_ms)
     if pg:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -309,6 +304,52 @@ def run_ours(args, rank, world, local):
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = world * N * args.steps / (total_ms / 1e3)
+
+    # ---- per-kernel durations for the roofline: the same steps with an event
+    # pair around every call (kernel time plus its own launch latency)
+    names = ["route", "dispatch", "combine"]
+    ksteps = min(args.steps, 1000)
+    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ksteps)]
+    for i in range(ksteps):
+        flush.zero_()
+        step(kevs[i])
+    torch.cuda.synchronize()
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+    t2 = time.time()
+    per = {n: [ev[j].elapsed_time(ev[j + 1]) for ev in kevs] for j, n in enumerate(names)}
+
+    # ---- the same step replayed from a CUDA graph (launch overhead removed)
+    graph = None
+    try:
+        gs = torch.cuda.Stream()
+        gsp = ctypes.c_void_p(gs.cuda_stream)
+        g_ws = moe.dispatch_workspace(E, dev, gs)
+        g_route = route_args[:-1] + (gsp,)
+        g_disp = disp_args[:-3] + (vp(g_ws), g_ws.numel(), gsp)
+        g_comb = comb_args[:-1] + (gsp,)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            for _ in range(2):  # warm the graph stream's workspace and plans
+                L.moe_route_ex(*g_route); L.moe_dispatch(*g_disp); L.moe_combine(*g_comb)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=gs):
+            rc = L.moe_route_ex(*g_route) | L.moe_dispatch(*g_disp) | L.moe_combine(*g_comb)
+        if rc:
+            raise RuntimeError(moe.status_string(rc))
+        gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ksteps)]
+        for i in range(ksteps):
+            flush.zero_()
+            gevs[i][0].record(stream)
+            cg.replay()
+            gevs[i][1].record(stream)
+        torch.cuda.synchronize()
+        g_ms = statistics.fmean(ev[0].elapsed_time(ev[1]) for ev in gevs)
+        graph = {"ms_per_step": g_ms, "tokens_per_s": N / (g_ms * 1e-3), "steps": ksteps}
+    except Exception as exc:  # graph capture is reported, not required
+        graph = {"error": str(exc)[:200]}
 
     # ---- end to end through the public API: pinned host X in, host out back, every step
     Xh = X.pin_memory()
@@ -362,7 +403,10 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": world * N / (e2e_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": N * H * 2,
                 "d2h_bytes_per_step": N * H * 2, "ms_per_step": e2e_mean,
                 "path": "pinned host X -> device, route, dispatch, permute, combine, out -> pinned host"},
-        "clocks": sampler.summary(t0, t1) if sampler else None,
+        "clocks": sampler.summary(t0, t2) if sampler else None,
+        "graph": graph,
+        "timing": ("value: K steps, one event pair per step; kernels: a second pass of min(K,1000) "
+                   "steps with an event pair per call"),
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

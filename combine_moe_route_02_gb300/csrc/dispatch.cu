@@ -305,40 +305,69 @@ __device__ __forceinline__ uint2 quant_chunk_e4m3(const uint4 &x, float &s_out)
 // A lane holds CPL 16-byte chunks of the row at once (chunk base + lane + 32 j),
 // so a whole row slice is in flight before any store; rows wider than
 // 32 * CPL chunks take several batches.
+template <int CPL>
+__device__ __forceinline__ void load_row_batch(const uint4 *__restrict__ src, int base, int chunks, int lane,
+                                               uint4 (&x)[CPL])
+{
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const int c = base + lane + 32 * j;
+        x[j] = c < chunks ? __ldcs(src + c) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+template <bool kFp8, int CPL>
+__device__ __forceinline__ void quant_row_batch(const uint4 (&x)[CPL], uint2 (&q)[kFp8 ? CPL : 1],
+                                                float (&sc)[kFp8 ? CPL : 1])
+{
+    if constexpr (kFp8) {
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) q[j] = quant_chunk_e4m3(x[j], sc[j]);
+    }
+}
+
+template <bool kBf16Out, bool kFp8, int CPL>
+__device__ __forceinline__ void store_row_batch(const uint4 (&x)[CPL], const uint2 (&q)[kFp8 ? CPL : 1],
+                                                const float (&sc)[kFp8 ? CPL : 1], int base, int my_row, int K,
+                                                int H, uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq,
+                                                float *__restrict__ Xs, int lane)
+{
+    const int chunks = H >> 3;
+    const int nb = H >> 7;
+    for (int k = 0; k < K; ++k) {
+        const int r = __shfl_sync(0xffffffffu, my_row, k);
+        if (r < 0) continue;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int c = base + lane + 32 * j;
+            if (c >= chunks) continue;
+            if constexpr (kBf16Out) __stcs(Xp + static_cast<int64_t>(r) * chunks + c, x[j]);
+            if constexpr (kFp8) {
+                __stcs(reinterpret_cast<uint2 *>(Xq + static_cast<int64_t>(r) * H) + c, q[j]);
+                if ((lane & 15) == 0) Xs[static_cast<int64_t>(r) * nb + (c >> 4)] = sc[j];
+            }
+        }
+    }
+}
+
+// Copy one token's row to its K destination rows (and/or quantise it), one
+// warp.  Lane k < K holds the destination row of slot k in `my_row` (-1: skip).
+// A lane holds CPL 16-byte chunks of the row at once (chunk base + lane + 32 j),
+// so a whole row slice is in flight before any store; rows wider than
+// 32 * CPL chunks take several batches.
 template <bool kBf16Out, bool kFp8, int CPL>
 __device__ __forceinline__ void copy_token_rows(const uint4 *__restrict__ src, int my_row, int K, int H,
                                                 uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq,
                                                 float *__restrict__ Xs, int lane)
 {
     const int chunks = H >> 3;  // 16-byte chunks per row
-    const int nb = H >> 7;      // 128-element blocks per row (fp8)
     for (int base = 0; base < chunks; base += 32 * CPL) {
         uint4 x[CPL];
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int c = base + lane + 32 * j;
-            x[j] = c < chunks ? __ldcs(src + c) : make_uint4(0, 0, 0, 0);
-        }
         uint2 q[kFp8 ? CPL : 1];
         float sc[kFp8 ? CPL : 1];
-        if constexpr (kFp8) {
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) q[j] = quant_chunk_e4m3(x[j], sc[j]);
-        }
-        for (int k = 0; k < K; ++k) {
-            const int r = __shfl_sync(0xffffffffu, my_row, k);
-            if (r < 0) continue;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                const int c = base + lane + 32 * j;
-                if (c >= chunks) continue;
-                if constexpr (kBf16Out) __stcs(Xp + static_cast<int64_t>(r) * chunks + c, x[j]);
-                if constexpr (kFp8) {
-                    __stcs(reinterpret_cast<uint2 *>(Xq + static_cast<int64_t>(r) * H) + c, q[j]);
-                    if ((lane & 15) == 0) Xs[static_cast<int64_t>(r) * nb + (c >> 4)] = sc[j];
-                }
-            }
-        }
+        load_row_batch<CPL>(src, base, chunks, lane, x);
+        quant_row_batch<kFp8, CPL>(x, q, sc);
+        store_row_batch<kBf16Out, kFp8, CPL>(x, q, sc, base, my_row, K, H, Xp, Xq, Xs, lane);
     }
 }
 
@@ -457,6 +486,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
     __syncthreads();
 
     pdl_wait_prior_grids();
+
+    // ---- each warp's first token row does not depend on the metadata: load
+    // (and quantise) it now, so its latency hides behind the counting phases
+    const int ntok = static_cast<int>(t1 - t0);
+    const int chunks = p.H >> 3;
+    const bool pre = (kBf16Out || kFp8) && warp < ntok && chunks <= 32 * CPL;
+    uint4 xpre[CPL];
+    uint2 qpre[kFp8 ? CPL : 1];
+    float spre[kFp8 ? CPL : 1];
+    if (pre) {
+        load_row_batch<CPL>(p.X + (t0 + warp) * chunks, 0, chunks, lane, xpre);
+        quant_row_batch<kFp8, CPL>(xpre, qpre, spre);
+    }
 
     // ---- stage the CTA's expert ids (0xFFFF: out of range)
     bool bad = false;
@@ -590,11 +632,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
     // ---- permute this CTA's tokens (rows from shared memory)
     if constexpr (kBf16Out || kFp8) {
         __syncthreads();
-        const int ntok = static_cast<int>(t1 - t0);
         for (int j = warp; j < ntok; j += kFusedWarps) {
             const int my_row = lane < K ? rows_s[j * K + lane] : -1;
-            copy_token_rows<kBf16Out, kFp8, CPL>(p.X + (t0 + j) * (p.H >> 3), my_row, K, p.H, p.Xp, p.Xq,
-                                                 p.Xs, lane);
+            if (j == warp && pre)
+                store_row_batch<kBf16Out, kFp8, CPL>(xpre, qpre, spre, 0, my_row, K, p.H, p.Xp, p.Xq, p.Xs, lane);
+            else
+                copy_token_rows<kBf16Out, kFp8, CPL>(p.X + (t0 + j) * chunks, my_row, K, p.H, p.Xp, p.Xq, p.Xs,
+                                                     lane);
         }
     }
     pdl_launch_dependents();
@@ -672,21 +716,22 @@ cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int
     uint4 *xp = static_cast<uint4 *>(X_perm);
     uint8_t *xq = static_cast<uint8_t *>(X_fp8);
     const int chunks = H / 8;
-    const int cpl = chunks > 256 ? 16 : chunks > 128 ? 8 : chunks > 64 ? 4 : chunks > 32 ? 2 : 1;
+    int cpl = chunks > 256 ? 16 : chunks > 128 ? 8 : chunks > 64 ? 4 : chunks > 32 ? 2 : 1;
+    if (X_fp8 && cpl > 8) cpl = 8;  // codes and scales stay live too
 #define MOE_PERMUTE_LAUNCH(B, F, C) \
     return cudaLaunchKernelEx(&cfg, permute_kernel<B, F, C>, x, row_map, N, H, K, xp, xq, X_scale, status)
-#define MOE_PERMUTE_CPL(B, F)                          \
+#define MOE_PERMUTE_CPL8(B, F)                         \
     switch (cpl) {                                     \
     case 1: MOE_PERMUTE_LAUNCH(B, F, 1);               \
     case 2: MOE_PERMUTE_LAUNCH(B, F, 2);               \
     case 4: MOE_PERMUTE_LAUNCH(B, F, 4);               \
-    case 8: MOE_PERMUTE_LAUNCH(B, F, 8);               \
-    default: MOE_PERMUTE_LAUNCH(B, F, 16);             \
+    default: MOE_PERMUTE_LAUNCH(B, F, 8);              \
     }
-    if (X_perm && X_fp8) MOE_PERMUTE_CPL(true, true)
-    if (X_fp8) MOE_PERMUTE_CPL(false, true)
-    MOE_PERMUTE_CPL(true, false)
-#undef MOE_PERMUTE_CPL
+    if (X_perm && X_fp8) MOE_PERMUTE_CPL8(true, true)
+    if (X_fp8) MOE_PERMUTE_CPL8(false, true)
+    if (cpl == 16) MOE_PERMUTE_LAUNCH(true, false, 16);
+    MOE_PERMUTE_CPL8(true, false)
+#undef MOE_PERMUTE_CPL8
 #undef MOE_PERMUTE_LAUNCH
 }
 
@@ -733,7 +778,12 @@ template <bool B, bool F>
 cudaError_t launch_fused_cpl(const FusedParams &p, int grid, size_t smem, cudaStream_t stream, int dev)
 {
     const int chunks = p.H / 8;
-    if (chunks > 128) return launch_fused_t<B, F, 8>(p, grid, smem, stream, dev);
+    // fp8 keeps codes and scales live too: at most 4 chunks per lane (128 registers at 512 threads)
+    if constexpr (!F) {
+        if (chunks > 128) return launch_fused_t<B, F, 8>(p, grid, smem, stream, dev);
+    } else {
+        if (chunks > 64) return launch_fused_t<B, F, 4>(p, grid, smem, stream, dev);
+    }
     if (chunks > 64) return launch_fused_t<B, F, 4>(p, grid, smem, stream, dev);
     if (chunks > 32) return launch_fused_t<B, F, 2>(p, grid, smem, stream, dev);
     return launch_fused_t<B, F, 1>(p, grid, smem, stream, dev);
