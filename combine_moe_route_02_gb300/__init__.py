@@ -42,7 +42,7 @@ _ALGOS = {"auto": ROUTE_AUTO, "tcgen05": ROUTE_TCGEN05, "simt": ROUTE_SIMT}
 ABI_VERSION = 1
 EXPORTED_SYMBOLS = (
     "moe_route", "moe_route_ex", "moe_dispatch_workspace_size", "moe_dispatch",
-    "moe_permute", "moe_combine", "moe_status_string", "moe_abi_version",
+    "moe_permute", "moe_combine", "moe_status_string", "moe_abi_version", "moe_dispatch_noalloc",
 )
 
 _lib = None

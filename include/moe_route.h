@@ -140,6 +140,34 @@ MOE_API moe_status moe_dispatch(const int32_t *topk_idx, const void *X,
                         moe_stream_t stream);
 
 /*
+ * moe_dispatch_noalloc -- moe_dispatch without a caller-provided workspace.
+ * The pages have no counterpart: this is a convenience of this library for
+ * callers that cannot allocate device memory when they dispatch -- engines that
+ * fix their whole device-memory plan up front and forbid later allocation,
+ * code running where cudaMalloc would block or synchronise the device, or C
+ * callers with no device allocator of their own.  The inputs and outputs are
+ * still the caller's (same meaning as in moe_dispatch); the scratch is a
+ * 1 MiB + 256 B array compiled into the library, which every GPU that loads
+ * the library holds until the process exits.  The call allocates and frees
+ * nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (with that device current) and caches it; make that first call before
+ *    any stream capture.
+ *  - Every call clears the array's barrier counters on `stream` and then uses
+ *    the whole array: calls that may overlap on the GPU (other streams, other
+ *    host threads) race on it and must be serialised by the caller.
+ *  - Limit: one CTA per SM and at most 16384 slots per CTA, i.e.
+ *    N*K <= 16384 * (number of SMs) (about 2.49 million slots on a 152-SM
+ *    GB300); larger calls return MOE_ERR_UNSUPPORTED and launch nothing.
+ */
+MOE_API moe_status moe_dispatch_noalloc(const int32_t *topk_idx, const void *X,
+                                int64_t N, int H, int E, int K,
+                                int32_t *expert_counts, int32_t *expert_offsets,
+                                int32_t *row_map, int32_t *src_slot,
+                                void *X_perm, void *X_fp8, float *X_scale,
+                                int32_t *status_word, moe_stream_t stream);
+
+/*
  * moe_permute -- the row permute of the dispatch, on its own.
  * The gathered_tokens input of forward_mlp on the PithTrain page
  * (§6.1 模型协议先行): X_perm[row_map[n*K+k], :] = X[n, :].
