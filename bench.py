@@ -62,6 +62,52 @@ def dist_env():
     return rank, world, local
 
 
+KERNEL_SOURCES = {"route": "route_tc.cu", "dispatch": "dispatch.cu", "combine": "combine.cu"}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+
+
+def source_digest(kernel: str) -> str:
+    import hashlib
+    path = os.path.join(ROOT, "combine_moe_route_02_gb300", "csrc", KERNEL_SOURCES[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) from the committed ncu summary, or
+    None when there is none for this kernel/workload or the kernel's source has
+    changed since it was taken (the summary records a digest of the source)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload:
+            try:
+                value = float(cells[2])
+            except ValueError:
+                continue
+            return value if cells[3] == source_digest(kernel) else None
+    return None
+
+
+def max_over_ranks(value: float, dist_mod=None, device=None) -> float:
+    """The largest `value` over all ranks (the job is as slow as its slowest rank)."""
+    if dist_mod is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tokens_per_s(world: int, tokens_per_rank: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank routes its own tokens_per_rank each step."""
+    return world * tokens_per_rank * steps / (total_ms / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -297,13 +343,9 @@ def run_ours(args, rank, world, local):
     t1 = time.time()
     assert st.item() == 0, moe.status_string(st.item())
     step_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
-    total_ms = sum(step_ms)
-    if pg:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), pg, dev)
     ms_per_step = total_ms / args.steps
-    value = world * N * args.steps / (total_ms / 1e3)
+    value = weak_scaling_tokens_per_s(world, N, args.steps, total_ms)
 
     # ---- per-kernel durations for the roofline: the same steps with an event
     # pair around every call (kernel time plus its own launch latency)
@@ -370,11 +412,7 @@ def run_ours(args, rank, world, local):
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_mean = statistics.fmean(e2e_ms)
-    if pg:
-        t = torch.tensor([e2e_mean], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_mean = float(t.item())
+    e2e_mean = max_over_ranks(statistics.fmean(e2e_ms), pg, dev)
 
     if rank != 0:
         pg.destroy_process_group()
@@ -391,7 +429,9 @@ def run_ours(args, rank, world, local):
     roof = {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
             "frac": kern[dom]["gbs"] / peak, "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
             if peak_src == "measured" else "fallback 6800 GB/s",
-            "traffic": None, "algorithmic_bytes_per_launch": kb[dom]}
+            "traffic": ncu_traffic(dom, w.name), "algorithmic_bytes_per_launch": kb[dom],
+            "traffic_source": "profiles/dram_traffic.md (ncu dram__bytes_read.sum + dram__bytes_write.sum per "
+                              "launch; null when absent or taken on an older source of the kernel)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -132,6 +132,9 @@ __global__ void __launch_bounds__(kMetaThreads, 1) dispatch_meta_kernel(
     if (tid == 0) sm.bad = 0;
     __syncthreads();
 
+    // a single cluster: the next kernel may start launching now (it still
+    // waits for this grid to complete)
+    pdl_launch_dependents();
     pdl_wait_prior_grids();
 
     // ---- stage the CTA's expert ids (independent loads, unrolled)
@@ -252,7 +255,6 @@ __global__ void __launch_bounds__(kMetaThreads, 1) dispatch_meta_kernel(
     }
 
     if (sm.bad && tid == 0) report_status(status, MOE_ERR_BAD_INDEX);
-    pdl_launch_dependents();
     cluster_wait_acquire();
 }
 
@@ -415,6 +417,7 @@ constexpr int kFusedThreads = 512;
 constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr int kFusedMaxSlots = 16384;   // slots per CTA staged in shared memory
 constexpr int kFusedMaxCtas = 1024;     // bound used to size the workspace
+constexpr int kHistBatch = 32;          // per-thread count loads in flight at once
 
 struct FusedParams {
     const int32_t *topk_idx;
@@ -485,6 +488,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
     if (tid == 0) sm.bad = 0;
     __syncthreads();
 
+    // One wave of CTAs (cooperative launch): the next kernel may start
+    // launching now; it still waits for this grid to complete.
+    pdl_launch_dependents();
     pdl_wait_prior_grids();
 
     // ---- each warp's first token row does not depend on the metadata: load
@@ -554,13 +560,32 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
         return;
     }
 
-    // ---- phase 2: grid-wide counts and this CTA's base rows (all CTAs' counts from L2)
-    for (int f = tid; f < static_cast<int>(G) * E; f += kFusedThreads) {
-        const int v = __ldcg(p.hist + f);
-        const int e = f % E;
-        const int cc = f / E;
-        atomicAdd(&sm.total[e], v);
-        if (cc < c) atomicAdd(&sm.before[e], v);
+    // ---- phase 2: grid-wide counts and this CTA's base rows (all CTAs' counts from L2).
+    // Thread (grp, e) sums rows grp, grp + groups, ... of column e; all of its
+    // loads are issued before the first add (one L2 round trip), then the
+    // per-group partials meet in shared memory.
+    {
+        const int groups = kFusedThreads / E;   // >= 2 (E <= 256)
+        const int e = tid % E;
+        const int grp = tid / E;
+        int tot = 0, bef = 0;
+        if (grp < groups) {
+            for (int c0 = grp; c0 < static_cast<int>(G); c0 += kHistBatch * groups) {
+                int v[kHistBatch];
+#pragma unroll
+                for (int i = 0; i < kHistBatch; ++i) {
+                    const int cc = c0 + i * groups;
+                    v[i] = cc < static_cast<int>(G) ? __ldcg(p.hist + static_cast<int64_t>(cc) * E + e) : 0;
+                }
+#pragma unroll
+                for (int i = 0; i < kHistBatch; ++i) {
+                    tot += v[i];
+                    bef += (c0 + i * groups < c) ? v[i] : 0;
+                }
+            }
+            atomicAdd(&sm.total[e], tot);
+            atomicAdd(&sm.before[e], bef);
+        }
     }
     __syncthreads();
     if (warp == 0) {
@@ -641,7 +666,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
                                                      lane);
         }
     }
-    pdl_launch_dependents();
 }
 
 int meta_cluster_size(int64_t S)

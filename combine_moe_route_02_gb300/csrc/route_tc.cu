@@ -255,13 +255,21 @@ __global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_cons
         tmem_alloc(&tail.tmem_base, p.tmem_cols);
         tmem_relinquish();
     }
-    // inputs may come from the previous kernel in the stream (programmatic launch)
-    pdl_wait_prior_grids();
-    for (int e = threadIdx.x; e < p.EP; e += kThreads) bias_s[e] = (p.bias != nullptr && e < E) ? p.bias[e] : 0.f;
+    // One wave of CTAs: the next kernel in the stream may start launching now
+    // (it still waits for this grid to complete before it reads anything).
+    pdl_launch_dependents();
     tc_fence_before_sync();
-    __syncthreads();
+    __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after_sync();
     const uint32_t tmem_base = tail.tmem_base;
+    // inputs may come from the previous kernel in the stream (programmatic launch)
+    pdl_wait_prior_grids();
+    if (warp != 0) {
+        // the producer starts streaming at once; the bias is needed by the epilogue only
+        for (int e = threadIdx.x - 32; e < p.EP; e += kThreads - 32)
+            bias_s[e] = (p.bias != nullptr && e < E) ? p.bias[e] : 0.f;
+        named_barrier_sync(5, kThreads - 32);
+    }
 
     bool acc_ok = false;  // split mode, epilogue threads: the partial accumulator is complete
     if (warp == 0) {
@@ -361,8 +369,27 @@ __global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_cons
                 float r = -INFINITY, z = 0.f;
                 const int c_end = min(E, h * nph + nph);
                 const uint32_t col_addr = lane_addr + static_cast<uint32_t>(b * p.NP);
+                int c = h * nph;
+                // 32 columns per TMEM round trip while they lie inside this half
 #pragma unroll 1
-                for (int c = h * nph; c < c_end; c += 8) {
+                for (; c + 32 <= c_end; c += 32) {
+                    float v[32];
+                    tmem_ld_32x32b_x32(col_addr + c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 32; t += 2) {
+                        const float x0 = logit_of(v[t], bias_s[c + t]);
+                        const float x1 = logit_of(v[t + 1], bias_s[c + t + 1]);
+                        topk_push<KMAX>(ak, ai, order_key(x0), c + t);
+                        topk_push<KMAX>(bk, bi, order_key(x1), c + t + 1);
+                        if (!p.renorm) {
+                            online_sumexp(x0, r, z);
+                            online_sumexp(x1, r, z);
+                        }
+                    }
+                }
+#pragma unroll 1
+                for (; c < c_end; c += 8) {
                     float v[8];
                     tmem_ld_32x32b_x8(col_addr + c, v);
                     tmem_ld_wait();
@@ -456,8 +483,17 @@ __global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_cons
             const uint32_t local = smem_u32(buf + (static_cast<int>(rank) * R + row % R) * RS);
             const uint32_t remote = dsmem_map(local, owner);
             const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            int c = h * nph;
 #pragma unroll 1
-            for (int c = h * nph; c < h * nph + nph; c += 8) {
+            for (; c + 32 <= h * nph + nph; c += 32) {
+                float v[32];
+                tmem_ld_32x32b_x32(lane_addr + c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < 32; g += 4) st_dsmem_v4(remote + (c + g) * 4, v[g], v[g + 1], v[g + 2], v[g + 3]);
+            }
+#pragma unroll 1
+            for (; c < h * nph + nph; c += 8) {
                 float v[8];
                 tmem_ld_32x32b_x8(lane_addr + c, v);
                 tmem_ld_wait();
@@ -543,7 +579,6 @@ __global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_cons
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
     if (threadIdx.x == 0 && tail.abort) report_status(p.status, MOE_ERR_TIMEOUT);
-    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
