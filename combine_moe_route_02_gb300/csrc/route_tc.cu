@@ -76,21 +76,24 @@ struct TcParams {
     int N, H, E, K, renorm;
     int EP, NP, stages, nsplit, kb_per, tiles;
     uint32_t tmem_cols;
-    uint32_t exch_off;  // byte offset of the epilogue exchange area (from the aligned base)
-    uint32_t tail_off;  // byte offset of TcSmemTail
+    uint32_t exch_off;     // byte offset of the epilogue exchange area (from the aligned base)
+    uint32_t win_off;      // byte offset of the per-token winning logits
+    uint32_t staging_off;  // split mode: byte offset of the DSMEM staging area
+    uint32_t tail_off;     // byte offset of TcSmemTail
 };
 
 // Row stride (floats) of the split-mode staging buffer: NP + 4 keeps rows
 // 16-byte aligned for vector DSMEM stores and spreads banks.
 __host__ __device__ constexpr int stage_row_floats(int NP) { return NP + 4; }
 
-// Epilogue exchange area: per column half a sorted list per token
-// (KMAX values + KMAX ids), per half and token the running (max, sum-exp),
-// and per token the final K logits.
-__host__ __device__ constexpr uint32_t exch_bytes(int kmax)
+// Epilogue exchange area (persistent mode): per column half a sorted list per
+// token (KMAX keys + KMAX ids) and the running (max, sum-exp); then, in both
+// modes, per token the final K logits.
+__host__ __device__ constexpr uint32_t exch_lists_bytes(int kmax)
 {
-    return static_cast<uint32_t>(2 * kBM * kmax * 8 + 2 * kBM * 2 * 4 + kBM * kmax * 4);
+    return static_cast<uint32_t>(2 * kBM * kmax * 8 + 2 * kBM * 2 * 4);
 }
+__host__ __device__ constexpr uint32_t win_bytes(int kmax) { return static_cast<uint32_t>(kBM * kmax * 4); }
 
 // Order-preserving int32 key of a logit: NaN counts as -inf, -0 as +0, and
 // keys compare like the floats.  kKeyEmpty (below the key of -inf) marks an
@@ -202,7 +205,7 @@ __device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float a, float b, flo
 }
 
 template <int KMAX, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+__global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                const __grid_constant__ CUtensorMap tmW,
                                                                const TcParams p)
 {
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_cons
     int *lst_k = reinterpret_cast<int *>(smem + p.exch_off);            // [2 halves][KMAX][128] keys
     int *lst_i = lst_k + 2 * kBM * KMAX;                                   // [2 halves][KMAX][128] ids
     float *lst_rz = reinterpret_cast<float *>(lst_i + 2 * kBM * KMAX);     // [2 halves][2][128]
-    float *win_v = lst_rz + 2 * kBM * 2;                                   // [KMAX][128]
+    float *win_v = reinterpret_cast<float *>(smem + p.win_off);            // [KMAX][128]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -261,6 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_cons
     tc_fence_before_sync();
     __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after_sync();
+    // split mode: announce that this CTA runs (peers wait for it before writing
+    // into its shared memory); the matching wait comes after the MMAs
+    if constexpr (SPLIT) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const uint32_t tmem_base = tail.tmem_base;
     // inputs may come from the previous kernel in the stream (programmatic launch)
     pdl_wait_prior_grids();
@@ -471,9 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1) route_tc_kernel(const __grid_cons
         const int S = p.nsplit;
         const int R = kBM / S;                          // tokens owned by each CTA of the cluster
         const int RS = stage_row_floats(p.NP);
-        float *buf = reinterpret_cast<float *>(smem);   // [S slices][R rows][RS], reuses the ring
+        float *buf = reinterpret_cast<float *>(smem + p.staging_off);  // [S slices][R rows][RS]
         __syncwarp();
-        cluster_sync_all();                             // #1: every CTA's ring is free
+        // every CTA of the cluster has started, so its staging area may be written
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
         if (warp >= 2 && acc_ok && nkb > 0) {
             const int q = warp & 3;
             const int h = (warp - 2) >> 2;
@@ -625,25 +632,35 @@ constexpr size_t kSmemLimit = 227 * 1024;
 // if larger, the split staging area), the exchange area, the tail and the bias.
 struct TcLayout {
     int stages;
-    uint32_t exch_off, tail_off;
+    uint32_t exch_off, win_off, staging_off, tail_off;
     size_t smem;
 };
 
-bool layout_for(int EP, int NP, int kmax, bool split, TcLayout &L)
+// Shared memory of a launch: 1 KiB alignment slack, the TMA ring, then
+// (split mode) the DSMEM staging area, the epilogue exchange area, the tail
+// and the bias.  Split CTAs run only kb_per K-steps, so their ring needs no
+// more stages than that; they prefer to fit two CTAs per SM.
+bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, TcLayout &L)
 {
     const size_t slot = kABytes + static_cast<size_t>(EP) * kBK * 2;
     const size_t staging = split ? static_cast<size_t>(kBM) * stage_row_floats(NP) * sizeof(float) : 0;
-    const size_t fixed = 1024 + exch_bytes(kmax) + sizeof(TcSmemTail) + sizeof(float) * EP;
-    for (int st = kMaxStages; st >= 2; --st) {
-        size_t area = static_cast<size_t>(st) * slot;
-        if (staging > area) area = staging;
-        area = (area + 1023) & ~size_t(1023);
-        if (fixed + area <= kSmemLimit) {
-            L.stages = st;
-            L.exch_off = static_cast<uint32_t>(area);
-            L.tail_off = static_cast<uint32_t>(area + exch_bytes(kmax));
-            L.smem = fixed + area;
-            return true;
+    const size_t exch = (split ? 0 : exch_lists_bytes(kmax)) + win_bytes(kmax);
+    const size_t fixed = 1024 + staging + exch + sizeof(TcSmemTail) + sizeof(float) * EP;
+    const int max_st = split ? (kb_per < kMaxStages ? (kb_per < 1 ? 1 : kb_per) : kMaxStages) : kMaxStages;
+    const int min_st = split ? 1 : 2;
+    const size_t budgets[2] = {split ? static_cast<size_t>(113 * 1024) : kSmemLimit, kSmemLimit};
+    for (size_t budget : budgets) {
+        for (int st = max_st; st >= min_st; --st) {
+            const size_t ring = (static_cast<size_t>(st) * slot + 1023) & ~size_t(1023);
+            if (fixed + ring <= budget) {
+                L.stages = st;
+                L.staging_off = static_cast<uint32_t>(ring);
+                L.exch_off = static_cast<uint32_t>(ring + staging);
+                L.win_off = static_cast<uint32_t>(ring + staging + (split ? 0 : exch_lists_bytes(kmax)));
+                L.tail_off = static_cast<uint32_t>(ring + staging + exch);
+                L.smem = fixed + ring;
+                return true;
+            }
         }
     }
     return false;
@@ -711,7 +728,7 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     q.tiles = static_cast<int>((a.N + kBM - 1) / kBM);
     const int nk = (a.H + kBK - 1) / kBK;
 
-    // split H over a cluster while the tiles alone leave SMs idle (one CTA per SM)
+    // split H over a cluster while the tiles alone leave SMs idle
     int S = 1;
     while (S < 8 && static_cast<int64_t>(q.tiles) * S * 2 <= sms && nk >= 2 * S) S *= 2;
 
@@ -721,14 +738,16 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
         if ((err = set_smem_attr<KMAX, true>(dev)) != cudaSuccess) return err;
         // every cluster must be resident at once (one wave), else use a smaller split
         for (; S > 1; S >>= 1) {
-            if (!layout_for(q.EP, q.NP, KMAX, true, L)) continue;
+            if (!layout_for(q.EP, q.NP, KMAX, true, (nk + S - 1) / S, L)) continue;
             if (max_active_clusters<KMAX>(L.smem, S, dev) >= q.tiles) break;
         }
     }
     const bool split = S > 1;
-    if (!layout_for(q.EP, q.NP, KMAX, split, L)) return cudaErrorInvalidConfiguration;
+    if (!layout_for(q.EP, q.NP, KMAX, split, (nk + S - 1) / S, L)) return cudaErrorInvalidConfiguration;
     q.stages = L.stages;
     q.exch_off = L.exch_off;
+    q.win_off = L.win_off;
+    q.staging_off = L.staging_off;
     q.tail_off = L.tail_off;
     q.nsplit = S;
     q.kb_per = (nk + S - 1) / S;
