@@ -58,6 +58,7 @@ def _load():
         lib.oracle_dispatch.argtypes = [P, I64, I64, I64, P, P, P, P]
         lib.oracle_permute.argtypes = [P, P, I64, I64, I64, P, P, P]
         lib.oracle_combine.argtypes = [P, P, P, I64, I64, I64, P]
+        lib.oracle_combine_residual.argtypes = [P, P, P, P, I64, I64, I64, P]
         lib.oracle_expert_fixture.argtypes = [P, P, I64, I64, I64, P]
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
@@ -163,6 +164,23 @@ def combine(Y_bits, row_map, topk_w):
     H = Y.shape[1]
     out = np.empty((N, H), np.uint16)
     _check(lib.oracle_combine(_ptr(Y), _ptr(rm), _ptr(w), N, H, K, _ptr(out)), "oracle_combine")
+    return out
+
+
+def combine_residual(Y_bits, row_map, topk_w, residual_bits):
+    """forward_aggregate: weighted gather plus the residual, one bf16 rounding: bits [N,H]."""
+    lib = _load()
+    Y = _c(Y_bits, np.uint16)
+    rm = _c(row_map, np.int32)
+    w = _c(topk_w, np.float32)
+    R = _c(residual_bits, np.uint16)
+    N, K = w.shape
+    H = Y.shape[1]
+    if R.shape != (N, H):
+        raise ValueError("residual must be [N,H]")
+    out = np.empty((N, H), np.uint16)
+    _check(lib.oracle_combine_residual(_ptr(Y), _ptr(rm), _ptr(w), _ptr(R), N, H, K, _ptr(out)),
+           "oracle_combine_residual")
     return out
 
 

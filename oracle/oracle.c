@@ -25,7 +25,8 @@
  *                 §7.2 架构感知的量化核 (_compute_fp8_scale: clamp amax at
  *                 1e-4, multiply by 1/448 in fp32, power-of-two ceiling by the
  *                 exponent-bump bit rule);
- *                 §6.1 模型协议先行 (forward_aggregate: weighted expert output).
+ *                 §6.1 模型协议先行 (forward_aggregate: weighted expert output
+ *                 plus the residual connection).
  *   [C++ trainer] devpress.csdn.net C++/CUDA LLM trainer page, §6.2 FP8量化格式
  *                 (E4M3: 1 sign, 4 exponent, 3 mantissa bits, range +-448).
  *
@@ -424,6 +425,37 @@ int oracle_combine(const uint16_t *Y, const int32_t *row_map, const float *w,
                 int64_t r = row_map[n * K + k];
                 acc += (double)w[n * K + k] * oracle_bf16_to_f64(Y[r * H + h]);
             }
+            out[n * H + h] = oracle_f64_to_bf16(acc);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Combine with the residual connection: the whole of forward_aggregate
+ * ([PithTrain] §6.1, "weighted expert output + residual connection"):
+ * out[n,h] = bf16_rne( sum_{k=0}^{K-1} w[n,k] * Y[row_map[n*K+k], h] + residual[n,h] )
+ * with the weighted sum and the addition in fp64 and one rounding at the end.
+ * residual bf16 [N,H].
+ */
+int oracle_combine_residual(const uint16_t *Y, const int32_t *row_map, const float *w,
+                            const uint16_t *residual, int64_t N, int64_t H, int64_t K,
+                            uint16_t *out)
+{
+    if (N < 0 || H <= 0 || K <= 0)
+        return ORACLE_BAD_ARG;
+    for (int64_t s = 0; s < N * K; ++s)
+        if (row_map[s] < 0 || row_map[s] >= N * K)
+            return ORACLE_BAD_INDEX;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                int64_t r = row_map[n * K + k];
+                acc += (double)w[n * K + k] * oracle_bf16_to_f64(Y[r * H + h]);
+            }
+            acc += oracle_bf16_to_f64(residual[n * H + h]);
             out[n * H + h] = oracle_f64_to_bf16(acc);
         }
     }

@@ -218,7 +218,8 @@ def test_permute_matches_oracle(N, H, K, fp8):
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("N,H,E,K,fp8,bf16", [(513, 1024, 16, 2, False, True), (300, 2048, 64, 8, True, True),
                                               (257, 384, 32, 3, True, False), (1, 8, 4, 1, False, True),
-                                              (20000, 256, 128, 8, True, True)])
+                                              (20000, 256, 128, 8, True, True), (30001, 512, 64, 2, False, True),
+                                              (12345, 1024, 32, 4, True, False)])
 def test_dispatch_with_rows_matches_oracle(N, H, E, K, fp8, bf16, fused):
     X = mi.random_bf16((N, H), seed=N + H + K, scale=2.0)
     idx = mi.random_topk_idx(N, E, K, seed=N + E)

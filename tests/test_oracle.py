@@ -345,6 +345,53 @@ def test_combine_matches_fp64_einsum_within_half_ulp():
     assert np.all(np.abs(out - ref) <= 0.5 * ulp)
 
 
+def test_combine_residual_single_rounding():
+    # forward_aggregate adds the residual before the one bf16 rounding:
+    # 1 + 2^-8 + 2^-10 - 2^-9 = 1 + 0.375 ulp -> 1.0 (rounding the weighted sum
+    # first would give 1 + 2^-7).  Second column: small integers and quarters,
+    # exactly representable, so the result is the exact value.
+    Y = to_bits([1.0, 3.0, 2.0 ** -8, -5.0, 2.0 ** -10, 7.0]).reshape(3, 2)
+    w = np.array([[1.0, 1.0, 1.0]], np.float32)
+    w2 = np.array([[0.5, 0.25, 1.0]], np.float32)
+    R = to_bits([-(2.0 ** -9), 4.0]).reshape(1, 2)
+    rm = np.array([0, 1, 2], np.int32)
+    out = widen(oracle.combine_residual(Y, rm, w, R)).ravel()
+    assert out[0] == 1.0
+    assert out[1] == 3.0 - 5.0 + 7.0 + 4.0
+    out2 = widen(oracle.combine_residual(Y, rm, w2, R)).ravel()
+    assert out2[1] == 0.5 * 3.0 + 0.25 * -5.0 + 7.0 + 4.0
+
+
+def test_combine_residual_matches_fp64_einsum_within_half_ulp():
+    N, H, E, K = 40, 64, 8, 4
+    Y = mi.random_bf16((N * K, H), seed=15)
+    R = mi.random_bf16((N, H), seed=16, scale=3.0)
+    w = mi.random_weights(N, K, seed=17).numpy()
+    idx = mi.random_topk_idx(N, E, K, seed=18).numpy()
+    _, _, row_map, _ = oracle.dispatch(idx, E)
+    out = widen(oracle.combine_residual(mi.bf16_bits(Y), row_map, w, mi.bf16_bits(R)))
+    Yd = widen(mi.bf16_bits(Y))
+    ref = np.einsum("nk,nkh->nh", w.astype(np.float64), Yd[row_map.reshape(N, K)]) + widen(mi.bf16_bits(R))
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0**-126))) - 7)
+    assert np.all(np.abs(out - ref) <= 0.5 * ulp)
+
+
+def test_combine_residual_special_cases():
+    N, H, E, K = 25, 32, 6, 3
+    Y = mi.bf16_bits(mi.random_bf16((N * K, H), seed=19))
+    R = mi.random_bf16((N, H), seed=20)
+    R[R == 0] = 1.0                       # keep -0 out: 0 + (-0) is +0
+    R = mi.bf16_bits(R)
+    idx = mi.random_topk_idx(N, E, K, seed=21).numpy()
+    _, _, row_map, _ = oracle.dispatch(idx, E)
+    w = mi.random_weights(N, K, seed=22).numpy()
+    # zero weights: the residual comes back bit for bit
+    assert np.array_equal(oracle.combine_residual(Y, row_map, np.zeros_like(w), R), R)
+    # zero residual: the plain weighted combine
+    assert np.array_equal(oracle.combine_residual(Y, row_map, w, np.zeros_like(R)),
+                          oracle.combine(Y, row_map, w))
+
+
 def test_expert_fixture_matches_torch_fp32():
     rows, H, E = 30, 16, 5
     Xp = mi.random_bf16((rows, H), seed=8)
