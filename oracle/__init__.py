@@ -68,6 +68,9 @@ def _load():
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_f64_to_e4m3_satfinite.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_e4m3_satfinite.restype = ctypes.c_uint8
+        lib.oracle_ue8m0_block_scale.argtypes = [ctypes.c_double]
+        lib.oracle_ue8m0_block_scale.restype = ctypes.c_uint8
+        lib.oracle_permute_ue8m0.argtypes = [P, P, I64, I64, I64, P, P]
         lib.oracle_fp8_block_scale.argtypes = [ctypes.c_double]
         lib.oracle_fp8_block_scale.restype = ctypes.c_float
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -152,6 +155,23 @@ def permute(X_bits, row_map, K, fp8=False):
     _check(lib.oracle_permute(_ptr(X), _ptr(rm), N, H, K, _ptr(Xp), _ptr(Xq), _ptr(Xs)),
            "oracle_permute")
     return (Xp, Xq, Xs) if fp8 else Xp
+
+
+def permute_ue8m0(X_bits, row_map, K):
+    """E4M3 copy with UE8M0 block scales: returns Xq uint8 [N*K,H], Xs uint8 [N*K,H/128]."""
+    lib = _load()
+    X = _c(X_bits, np.uint16)
+    rm = _c(row_map, np.int32)
+    N, H = X.shape
+    Xq = np.empty((N * K, H), np.uint8)
+    Xs = np.empty((N * K, H // 128), np.uint8)
+    _check(lib.oracle_permute_ue8m0(_ptr(X), _ptr(rm), N, H, K, _ptr(Xq), _ptr(Xs)), "oracle_permute_ue8m0")
+    return Xq, Xs
+
+
+def ue8m0_block_scale(amax):
+    """UE8M0 scale byte of one block with absolute maximum `amax`."""
+    return int(_load().oracle_ue8m0_block_scale(float(amax)))
 
 
 def combine(Y_bits, row_map, topk_w):

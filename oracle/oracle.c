@@ -24,7 +24,8 @@
  *                 (histogram -> prefix sum -> scatter + expand_idx);
  *                 §7.2 架构感知的量化核 (_compute_fp8_scale: clamp amax at
  *                 1e-4, multiply by 1/448 in fp32, power-of-two ceiling by the
- *                 exponent-bump bit rule);
+ *                 exponent-bump bit rule, or, on the e8m0 branch, rounding
+ *                 toward +infinity to a UE8M0 exponent byte);
  *                 §6.1 模型协议先行 (forward_aggregate: weighted expert output
  *                 plus the residual connection).
  *   [C++ trainer] devpress.csdn.net C++/CUDA LLM trainer page, §6.2 FP8量化格式
@@ -189,6 +190,35 @@ float oracle_fp8_block_scale(double amax)
     uint32_t mant = bits & 0x007FFFFFu;
     uint32_t sbits = (bits & 0x7F800000u) + (mant != 0 ? 0x00800000u : 0u);
     return f32_from_bits(sbits);
+}
+
+/*
+ * The e8m0 branch of the same rule ([PithTrain] §7.2, _compute_fp8_scale with
+ * SCALING_MODE "e8m0", the Blackwell path): the same fp32 product t, rounded
+ * toward +infinity to a power of two 2^u, kept as the UE8M0 byte u + 127
+ * (unsigned, 8 exponent bits, no mantissa; 0xFF is NaN), saturating at the
+ * largest finite value 2^127 (byte 254).  The block scale is 2^(byte - 127).
+ */
+uint8_t oracle_ue8m0_block_scale(double amax)
+{
+    float a = (float)amax;
+    float lo = (float)1e-4;
+    float amax_clamped = a > lo ? a : lo;
+    float rcp = (float)(1.0 / 448.0);
+    double t = (double)(float)((double)amax_clamped * (double)rcp);
+    if (isnan(t))
+        return 0xFF;
+    if (isinf(t))
+        return 254;
+    int ex;
+    double m = frexp(t, &ex);          /* t = m * 2^ex, 0.5 <= m < 1 */
+    int u = (m == 0.5) ? ex - 1 : ex;  /* smallest power of two >= t */
+    int b = u + 127;
+    if (b > 254)
+        b = 254;
+    if (b < 0)
+        b = 0;
+    return (uint8_t)b;
 }
 
 /* ------------------------------------------------------------------ */
@@ -394,6 +424,46 @@ int oracle_permute(const uint16_t *X, const int32_t *row_map,
                         double x = oracle_bf16_to_f64(X[n * H + b * 128 + j]);
                         Xq[r * H + b * 128 + j] = oracle_f64_to_e4m3_satfinite(x / (double)s);
                     }
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * The E4M3 copy of the permute with UE8M0 block scales (the e8m0 branch):
+ * for every 1x128 block b of X[n,:], byte = oracle_ue8m0_block_scale(max |x|),
+ * s = 2^(byte - 127), q = E4M3(x / s); both written to each of the token's K
+ * destination rows.  Xq [N*K, H], Xs8 [N*K, H/128] one byte per block.
+ */
+int oracle_permute_ue8m0(const uint16_t *X, const int32_t *row_map,
+                         int64_t N, int64_t H, int64_t K,
+                         uint8_t *Xq, uint8_t *Xs8)
+{
+    if (N < 0 || H <= 0 || K <= 0 || H % 128 != 0 || !Xq || !Xs8)
+        return ORACLE_BAD_ARG;
+    int64_t nb = H / 128;
+    for (int64_t s = 0; s < N * K; ++s)
+        if (row_map[s] < 0 || row_map[s] >= N * K)
+            return ORACLE_BAD_INDEX;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t r = row_map[n * K + k];
+            for (int64_t b = 0; b < nb; ++b) {
+                double amax = 0.0;
+                for (int64_t j = 0; j < 128; ++j) {
+                    double v = fabs(oracle_bf16_to_f64(X[n * H + b * 128 + j]));
+                    if (v > amax)
+                        amax = v;
+                }
+                uint8_t e = oracle_ue8m0_block_scale(amax);
+                double sc = ldexp(1.0, (int)e - 127);
+                Xs8[r * nb + b] = e;
+                for (int64_t j = 0; j < 128; ++j) {
+                    double x = oracle_bf16_to_f64(X[n * H + b * 128 + j]);
+                    Xq[r * H + b * 128 + j] = oracle_f64_to_e4m3_satfinite(x / sc);
                 }
             }
         }

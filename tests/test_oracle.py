@@ -117,6 +117,38 @@ def test_fp8_block_scale_is_smallest_pow2_not_below_t():
         assert s >= t and s / 2 < t, (amax, s, t)
 
 
+def test_ue8m0_block_scale_golden():
+    for amax, b in read_golden("ue8m0_block_scale.txt"):
+        assert oracle.ue8m0_block_scale(float(amax)) == int(b), amax
+
+
+def test_ue8m0_block_scale_rounds_up_and_matches_fp32_branch():
+    # closed form of round-toward-+inf to a power of two: 2^(b-127) >= t > 2^(b-128);
+    # and the two branches of the page's rule give the same scale value
+    rng = np.random.default_rng(3)
+    for amax in np.concatenate([rng.uniform(0, 10, 500), 10.0 ** rng.uniform(-6, 30, 500)]):
+        b = oracle.ue8m0_block_scale(float(amax))
+        a = max(np.float32(amax), np.float32(1e-4))
+        t = float(np.float32(a) * np.float32(1.0 / 448.0))
+        assert 2.0 ** (b - 127) >= t and 2.0 ** (b - 128) < t, (amax, b, t)
+        assert 2.0 ** (b - 127) == oracle.fp8_block_scale(float(amax))
+
+
+def test_permute_ue8m0_matches_fp32_scale_path():
+    N, H, E, K = 30, 384, 8, 3
+    X = mi.random_bf16((N, H), seed=31, scale=3.0)
+    X[0, :128] = 0.0
+    X[1, 128:256] *= 1e-6
+    X[2, 256:] *= 500.0
+    idx = mi.random_topk_idx(N, E, K, seed=32).numpy()
+    _, _, row_map, _ = oracle.dispatch(idx, E)
+    _, Xq, Xs = oracle.permute(mi.bf16_bits(X), row_map, K, fp8=True)
+    Xq8, Xs8 = oracle.permute_ue8m0(mi.bf16_bits(X), row_map, K)
+    assert Xs8.dtype == np.uint8
+    assert np.array_equal(Xq8, Xq)
+    assert np.array_equal(np.ldexp(1.0, Xs8.astype(np.int32) - 127), Xs.astype(np.float64))
+
+
 # ---------------------------------------------------------------- route
 
 def test_route_golden_ties():
