@@ -52,6 +52,10 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--scale-format", default="fp32", choices=["fp32", "ue8m0"],
+                   help="E4M3 block-scale output of fp8 workloads: fp32 scales or UE8M0 exponent bytes")
+    p.add_argument("--residual", action="store_true",
+                   help="combine with the residual connection (forward_aggregate: moe_combine_residual)")
     return p.parse_args()
 
 
@@ -120,14 +124,16 @@ def measured_peaks():
 
 # ----------------------------------------------------------------- algorithmic bytes per launch
 
-def kernel_bytes(w: mi.Workload):
+def kernel_bytes(w: mi.Workload, residual: bool = False, ue8m0: bool = False):
     N, H, E, K = w.N, w.H, w.E, w.K
     route = N * 2 * H + H * E * 2 + N * K * 8 + (E * 4 if w.skew else 0)
     meta = N * K * 4 * 3                      # read topk_idx, write row_map and src_slot
     permute = N * 2 * H + N * K * 2 * H       # read X once, write K rows (bf16)
     if w.fp8:
-        permute += N * K * H + N * K * (H // 128) * 4
+        permute += N * K * H + N * K * (H // 128) * (1 if ue8m0 else 4)
     combine = N * K * 2 * H + N * 2 * H + N * K * 8
+    if residual:
+        combine += N * 2 * H                  # read the residual row
     return {"route": route, "dispatch": meta + permute, "combine": combine}
 
 
@@ -195,25 +201,40 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- CPU oracle baseline
 
-def oracle_pass(oracle, Xb, Wb, bias, w: mi.Workload, Y):
-    """One pass of the oracle over the workload: route, dispatch, permute, combine."""
+def oracle_pass(oracle, Xb, Wb, bias, w: mi.Workload, Y, R=None, ue8m0=False):
+    """One pass of the oracle over the workload: route, dispatch, permute, combine
+    (with the residual R when given; UE8M0 block scales when ue8m0)."""
     idx, tw = oracle.route(Xb, Wb, bias, w.K, w.renorm)
     counts, offsets, row_map, src_slot = oracle.dispatch(idx, w.E)
-    oracle.permute(Xb, row_map, w.K, fp8=w.fp8)
-    oracle.combine(Y, row_map, tw)
+    if w.fp8 and ue8m0:
+        oracle.permute(Xb, row_map, w.K)
+        oracle.permute_ue8m0(Xb, row_map, w.K)
+    else:
+        oracle.permute(Xb, row_map, w.K, fp8=w.fp8)
+    if R is None:
+        oracle.combine(Y, row_map, tw)
+    else:
+        oracle.combine_residual(Y, row_map, tw, R)
     return idx
 
 
-def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000):
+def residual_rows(w: mi.Workload, rank: int = 0):
+    """Synthetic residual stream [N,H] bf16 for the forward_aggregate variant."""
+    return mi.random_bf16((w.N, w.H), seed=1000 + rank)
+
+
+def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000, residual: bool = False,
+                 ue8m0: bool = False):
     import oracle
     X, W, bias = mi.make_workload_inputs(w)
     Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
     b = None if bias is None else bias.numpy()
     r = oracle.run_path(Xb, Wb, b, w.K, w.renorm, w.fp8)   # untimed: provides the expert outputs Y
     Y = r["Y"]
+    R = mi.bf16_bits(residual_rows(w)) if residual else None
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle_pass(oracle, Xb, Wb, b, w, Y)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= max_reps:
@@ -232,22 +253,32 @@ def run_reference(args, rank, world):
     Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
     b = None if bias is None else bias.numpy()
     Y = oracle.run_path(Xb, Wb, b, w.K, w.renorm, w.fp8)["Y"]
+    R = mi.bf16_bits(residual_rows(w)) if args.residual else None
+    ue8m0 = args.scale_format == "ue8m0"
     for _ in range(args.warmup):
-        oracle_pass(oracle, Xb, Wb, b, w, Y)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_pass(oracle, Xb, Wb, b, w, Y)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0)
     el = time.perf_counter() - t0
     value = args.steps * w.N / el
     sample = f"the whole {w.name} workload ({w.N} tokens) per step, fp64 C oracle"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": w.as_dict(),
+            "data": "synthetic", "config": dict(w.as_dict(), **combine_config(args)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def combine_config(args):
+    c = {"combine": "forward_aggregate: weighted sum + residual, one bf16 rounding" if args.residual
+         else "weighted sum"}
+    if mi.WORKLOADS[args.workload].fp8:
+        c["fp8_scales"] = args.scale_format
+    return c
 
 
 # ----------------------------------------------------------------- the GPU arm
@@ -277,12 +308,14 @@ def run_ours(args, rank, world, local):
     idx = torch.empty((N, K), dtype=torch.int32, device=dev)
     tw = torch.empty((N, K), dtype=torch.float32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    d = moe.dispatch(moe.route(Xd, Wd, K, bd, w.renorm, topk_idx=idx, topk_w=tw)[0], E, Xd, fp8=w.fp8)
+    d = moe.dispatch(moe.route(Xd, Wd, K, bd, w.renorm, topk_idx=idx, topk_w=tw)[0], E, Xd, fp8=w.fp8,
+                     scale_format=args.scale_format)
     # expert outputs for the combine: synthetic stand-in built once (untimed)
     expert = torch.repeat_interleave(torch.arange(E, device=dev), d.expert_counts.to(torch.int64))
     scale = torch.tensor([np.float32(1.0 + e / E) for e in range(E)], dtype=torch.float32, device=dev)
     Y = (d.X_perm.float() * scale[expert][:, None]).to(torch.bfloat16)
     out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    R = residual_rows(w, rank).to(dev) if args.residual else None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -293,9 +326,15 @@ def run_ours(args, rank, world, local):
     vp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     sp = ctypes.c_void_p(stream.cuda_stream)
     route_args = (vp(Xd), vp(Wd), vp(bd), N, H, E, K, int(w.renorm), vp(idx), vp(tw), vp(st), moe.ROUTE_AUTO, sp)
+    fmt = moe.SCALE_UE8M0 if args.scale_format == "ue8m0" else moe.SCALE_FP32
     disp_args = (vp(idx), vp(Xd), N, H, E, K, vp(d.expert_counts), vp(d.expert_offsets), vp(d.row_map),
-                 vp(d.src_slot), vp(d.X_perm), vp(d.X_fp8), vp(d.X_scale), vp(st), vp(ws), ws.numel(), sp)
-    comb_args = (vp(Y), vp(d.row_map), vp(tw), N, H, K, vp(out), vp(st), sp)
+                 vp(d.src_slot), vp(d.X_perm), vp(d.X_fp8), vp(d.X_scale), fmt, vp(st), vp(ws), ws.numel(), sp)
+    if R is None:
+        comb_fn = L.moe_combine
+        comb_args = (vp(Y), vp(d.row_map), vp(tw), N, H, K, vp(out), vp(st), sp)
+    else:
+        comb_fn = L.moe_combine_residual
+        comb_args = (vp(Y), vp(d.row_map), vp(tw), vp(R), N, H, K, vp(out), vp(st), sp)
 
     def step(ev=None):
         rc = 0
@@ -304,10 +343,10 @@ def run_ours(args, rank, world, local):
         rc |= L.moe_route_ex(*route_args)
         if ev is not None:
             ev[1].record(stream)
-        rc |= L.moe_dispatch(*disp_args)           # counting sort + row permute (+ E4M3), one launch
+        rc |= L.moe_dispatch_ex(*disp_args)        # counting sort + row permute (+ E4M3), one launch
         if ev is not None:
             ev[2].record(stream)
-        rc |= L.moe_combine(*comb_args)
+        rc |= comb_fn(*comb_args)
         if ev is not None:
             ev[3].record(stream)
         if rc:
@@ -374,11 +413,11 @@ def run_ours(args, rank, world, local):
         gs.wait_stream(stream)
         with torch.cuda.stream(gs):
             for _ in range(2):  # warm the graph stream's workspace and plans
-                L.moe_route_ex(*g_route); L.moe_dispatch(*g_disp); L.moe_combine(*g_comb)
+                L.moe_route_ex(*g_route); L.moe_dispatch_ex(*g_disp); comb_fn(*g_comb)
         torch.cuda.synchronize()
         cg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg, stream=gs):
-            rc = L.moe_route_ex(*g_route) | L.moe_dispatch(*g_disp) | L.moe_combine(*g_comb)
+            rc = L.moe_route_ex(*g_route) | L.moe_dispatch_ex(*g_disp) | comb_fn(*g_comb)
         if rc:
             raise RuntimeError(moe.status_string(rc))
         gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ksteps)]
@@ -419,7 +458,7 @@ def run_ours(args, rank, world, local):
         return
 
     peak, peak_src = measured_peaks()
-    kb = kernel_bytes(w)
+    kb = kernel_bytes(w, args.residual, args.scale_format == "ue8m0")
     kern = {}
     for n in names:
         ms = statistics.fmean(per[n])
@@ -437,7 +476,8 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(w.as_dict(), l2="256 MiB buffer written before every timed step (L2 flush)",
+        "config": dict(w.as_dict(), **combine_config(args),
+                       l2="256 MiB buffer written before every timed step (L2 flush)",
                        accumulate="fp32", parallelism="replicas: each GPU routes its own tokens, no collective"),
         "roofline": roof, "kernels": kern, "gpu_launches": kernels_per_step * args.steps,
         "e2e": {"value": world * N / (e2e_mean / 1e3), "unit": UNIT, "h2d_bytes_per_step": N * H * 2,
@@ -449,7 +489,8 @@ def run_ours(args, rank, world, local):
                    "steps with an event pair per call"),
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, residual=args.residual,
+                                            ue8m0=args.scale_format == "ue8m0")
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()

@@ -43,7 +43,21 @@ ABI_VERSION = 1
 EXPORTED_SYMBOLS = (
     "moe_route", "moe_route_ex", "moe_dispatch_workspace_size", "moe_dispatch",
     "moe_permute", "moe_combine", "moe_status_string", "moe_abi_version", "moe_dispatch_noalloc",
+    "moe_combine_residual", "moe_dispatch_ex", "moe_permute_ex",
 )
+
+SCALE_FP32, SCALE_UE8M0 = 0, 1
+_SCALE_FORMATS = {"fp32": SCALE_FP32, "ue8m0": SCALE_UE8M0}
+
+
+def _scale_format(name: str) -> int:
+    if name not in _SCALE_FORMATS:
+        raise ValueError(f"scale_format must be one of {sorted(_SCALE_FORMATS)}")
+    return _SCALE_FORMATS[name]
+
+
+def _scale_dtype(name: str):
+    return torch.uint8 if name == "ue8m0" else torch.float32
 
 _lib = None
 
@@ -82,6 +96,12 @@ def lib():
     L.moe_permute.restype = I32
     L.moe_combine.argtypes = [P, P, P, I64, I32, I32, P, P, P]
     L.moe_combine.restype = I32
+    L.moe_combine_residual.argtypes = [P, P, P, P, I64, I32, I32, P, P, P]
+    L.moe_combine_residual.restype = I32
+    L.moe_dispatch_ex.argtypes = [P, P, I64, I32, I32, I32, P, P, P, P, P, P, P, I32, P, P, SZ, P]
+    L.moe_dispatch_ex.restype = I32
+    L.moe_permute_ex.argtypes = [P, P, I64, I32, I32, P, P, P, I32, P, P]
+    L.moe_permute_ex.restype = I32
     L.moe_status_string.argtypes = [I32]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_abi_version.argtypes = []
@@ -189,13 +209,15 @@ def dispatch_workspace(E: int, device=None, stream=None) -> torch.Tensor:
 def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, fp8: bool = False,
              bf16: bool = True, want_src_slot: bool = True, out: Optional[Dispatch] = None,
              workspace: Optional[torch.Tensor] = None, fused: bool = True, status=None,
-             stream=None) -> Dispatch:
+             stream=None, scale_format: str = "fp32") -> Dispatch:
     """Counting-sort dispatch (+ optional row permute / E4M3 quantise).
 
     fused=True (default) runs the one-launch cooperative kernel with a
     workspace (a cached zeroed one unless given); fused=False passes no
     workspace, which selects the single-cluster metadata kernel followed by
-    the permute kernel."""
+    the permute kernel.  scale_format "fp32" (float scales) or "ue8m0" (one
+    exponent byte per 1x128 block) selects the E4M3 block-scale output."""
+    fmt = _scale_format(scale_format)
     N, K = topk_idx.shape
     _need(topk_idx, "topk_idx", torch.int32)
     dev = topk_idx.device
@@ -213,7 +235,7 @@ def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, f
             src_slot=torch.empty(N * K, dtype=torch.int32, device=dev) if want_src_slot else None,
             X_perm=torch.empty((N * K, H), dtype=torch.bfloat16, device=dev) if (X is not None and bf16) else None,
             X_fp8=torch.empty((N * K, H), dtype=torch.uint8, device=dev) if (X is not None and fp8) else None,
-            X_scale=torch.empty((N * K, H // 128), dtype=torch.float32, device=dev)
+            X_scale=torch.empty((N * K, H // 128), dtype=_scale_dtype(scale_format), device=dev)
             if (X is not None and fp8) else None,
         )
     if not fused:
@@ -221,18 +243,20 @@ def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, f
     elif workspace is None:
         workspace = dispatch_workspace(E, dev, stream)
     has_x = X is not None
-    code = lib().moe_dispatch(
+    code = lib().moe_dispatch_ex(
         _ptr(topk_idx), _ptr(X), N, H, E, K, _ptr(out.expert_counts), _ptr(out.expert_offsets),
         _ptr(out.row_map), _ptr(out.src_slot), _ptr(out.X_perm) if has_x else None,
-        _ptr(out.X_fp8) if has_x else None, _ptr(out.X_scale) if has_x else None,
+        _ptr(out.X_fp8) if has_x else None, _ptr(out.X_scale) if has_x else None, fmt,
         _ptr(status), _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
-    _check(code, "moe_dispatch")
+    _check(code, "moe_dispatch_ex")
     return out
 
 
 def permute(X: torch.Tensor, row_map: torch.Tensor, K: int, bf16: bool = True, fp8: bool = False,
-            X_perm=None, X_fp8=None, X_scale=None, status=None, stream=None):
-    """Row permute: returns (X_perm, X_fp8, X_scale) (entries None when not requested)."""
+            X_perm=None, X_fp8=None, X_scale=None, status=None, stream=None, scale_format: str = "fp32"):
+    """Row permute: returns (X_perm, X_fp8, X_scale) (entries None when not requested);
+    X_scale is fp32, or uint8 UE8M0 bytes with scale_format="ue8m0"."""
+    fmt = _scale_format(scale_format)
     N, H = X.shape
     _need(X, "X", torch.bfloat16)
     _need(row_map, "row_map", torch.int32, (N * K,))
@@ -241,16 +265,18 @@ def permute(X: torch.Tensor, row_map: torch.Tensor, K: int, bf16: bool = True, f
         X_perm = torch.empty((N * K, H), dtype=torch.bfloat16, device=dev)
     if fp8 and X_fp8 is None:
         X_fp8 = torch.empty((N * K, H), dtype=torch.uint8, device=dev)
-        X_scale = torch.empty((N * K, H // 128), dtype=torch.float32, device=dev)
-    code = lib().moe_permute(_ptr(X), _ptr(row_map), N, H, K, _ptr(X_perm), _ptr(X_fp8), _ptr(X_scale),
-                             _ptr(status), _stream(stream))
-    _check(code, "moe_permute")
+        X_scale = torch.empty((N * K, H // 128), dtype=_scale_dtype(scale_format), device=dev)
+    code = lib().moe_permute_ex(_ptr(X), _ptr(row_map), N, H, K, _ptr(X_perm), _ptr(X_fp8), _ptr(X_scale), fmt,
+                                _ptr(status), _stream(stream))
+    _check(code, "moe_permute_ex")
     return X_perm, X_fp8, X_scale
 
 
 def combine(Y: torch.Tensor, row_map: torch.Tensor, topk_w: torch.Tensor, out=None, status=None,
-            stream=None) -> torch.Tensor:
-    """Weighted gather back to token order: out bf16 [N,H]."""
+            stream=None, residual=None) -> torch.Tensor:
+    """Weighted gather back to token order: out bf16 [N,H]; with `residual`
+    (bf16 [N,H]) the residual is added before the bf16 rounding
+    (moe_combine_residual).  `out` may be `residual` itself (in place)."""
     N, K = topk_w.shape
     H = Y.shape[1]
     _need(Y, "Y", torch.bfloat16, (N * K, H))
@@ -259,7 +285,13 @@ def combine(Y: torch.Tensor, row_map: torch.Tensor, topk_w: torch.Tensor, out=No
     if out is None:
         out = torch.empty((N, H), dtype=torch.bfloat16, device=Y.device)
     _need(out, "out", torch.bfloat16, (N, H))
-    code = lib().moe_combine(_ptr(Y), _ptr(row_map), _ptr(topk_w), N, H, K, _ptr(out), _ptr(status),
-                             _stream(stream))
-    _check(code, "moe_combine")
+    if residual is None:
+        code = lib().moe_combine(_ptr(Y), _ptr(row_map), _ptr(topk_w), N, H, K, _ptr(out), _ptr(status),
+                                 _stream(stream))
+        _check(code, "moe_combine")
+    else:
+        _need(residual, "residual", torch.bfloat16, (N, H))
+        code = lib().moe_combine_residual(_ptr(Y), _ptr(row_map), _ptr(topk_w), _ptr(residual), N, H, K,
+                                          _ptr(out), _ptr(status), _stream(stream))
+        _check(code, "moe_combine_residual")
     return out

@@ -1,11 +1,15 @@
 // combine.cu -- weighted gather of the K expert rows of every token back to
-// token order (the weighted part of forward_aggregate, PithTrain page
+// token order (forward_aggregate, PithTrain page
 // "一万行Python构建MoE训练栈：解构4D并行、DualPipeV调度与FP8算子",
-// §6.1 模型协议先行):  out[n,:] = sum_k w[n,k] * Y[row_map[n*K+k], :].
+// §6.1 模型协议先行):  out[n,:] = sum_k w[n,k] * Y[row_map[n*K+k], :], and,
+// with the residual connection of the same method, + residual[n,:].
 //
 // One warp per token, 16-byte vectors: every lane gathers the same 16-byte
-// column chunk from the K rows (independent loads, all in flight together),
-// accumulates in fp32 in k order, rounds to bf16 (nearest even) and stores.
+// column chunk from the K rows (independent loads, all in flight together,
+// with the residual chunk), accumulates in fp32 in k order, adds the residual,
+// rounds to bf16 (nearest even) and stores.  A lane reads its residual chunk
+// before it writes the same chunk of out, so out may be the residual buffer
+// itself (an in-place update of the residual stream).
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -35,13 +39,25 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8])
     return o;
 }
 
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &r)
+{
+    const uint32_t v[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        acc[2 * p] += __uint_as_float(v[p] << 16);
+        acc[2 * p + 1] += __uint_as_float(v[p] & 0xFFFF0000u);
+    }
+}
+
 // KT > 0: K known at compile time -- every lane issues the loads of CPL
 // chunks x KT rows before the first FMA (CPL * KT <= 16 uint4 in flight per
-// lane).  KT == 0: runtime K, one chunk at a time.
-template <int KT, int CPL>
+// lane).  KT == 0: runtime K, one chunk at a time.  RES: add residual[n,:]
+// after the weighted sum (out and residual may be the same buffer, so
+// neither is declared restrict).
+template <int KT, int CPL, bool RES>
 __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
     const uint4 *__restrict__ Y, const int32_t *__restrict__ row_map, const float *__restrict__ w, int64_t N,
-    int H, int K_rt, uint4 *__restrict__ out, int32_t *status)
+    int H, int K_rt, const uint4 *residual, uint4 *out, int32_t *status)
 {
     const int K = KT > 0 ? KT : K_rt;
     const int warp = threadIdx.x >> 5;
@@ -66,6 +82,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
             }
         }
         uint4 *dst = out + n * chunks;
+        const uint4 *res = RES ? residual + n * chunks : nullptr;
         if constexpr (KT > 0) {
             const uint4 *yr[KT];
             float wk[KT];
@@ -76,11 +93,13 @@ __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
             }
             for (int base = 0; base < chunks; base += 32 * CPL) {
                 uint4 y[CPL][KT];
+                uint4 rr[RES ? CPL : 1];
 #pragma unroll
                 for (int j = 0; j < CPL; ++j) {
                     const int c = base + lane + 32 * j;
 #pragma unroll
                     for (int k = 0; k < KT; ++k) y[j][k] = c < chunks ? __ldcs(yr[k] + c) : make_uint4(0, 0, 0, 0);
+                    if constexpr (RES) rr[j] = c < chunks ? __ldcs(res + c) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
                 for (int j = 0; j < CPL; ++j) {
@@ -88,6 +107,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
                     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int k = 0; k < KT; ++k) fma_bf16x8(acc, y[j][k], wk[k]);
+                    if constexpr (RES) add_bf16x8(acc, rr[j]);
                     if (c < chunks) __stcs(dst + c, pack_bf16x8(acc));
                 }
             }
@@ -100,6 +120,9 @@ __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
                     const int r = __shfl_sync(0xffffffffu, my_row, k);
                     const float wk = __shfl_sync(0xffffffffu, my_w, k);
                     if (v) fma_bf16x8(acc, __ldcs(Y + static_cast<int64_t>(r) * chunks + c), wk);
+                }
+                if constexpr (RES) {
+                    if (v) add_bf16x8(acc, __ldcs(res + c));
                 }
                 if (v) __stcs(dst + c, pack_bf16x8(acc));
             }
@@ -118,8 +141,9 @@ int pow2_chunks_per_lane(int chunks, int cap)
 
 }  // namespace
 
-cudaError_t launch_combine(const void *Y, const int32_t *row_map, const float *w, int64_t N, int H, int K,
-                           void *out, int32_t *status, cudaStream_t stream)
+template <bool RES>
+cudaError_t launch_combine_t(const void *Y, const int32_t *row_map, const float *w, const void *residual,
+                             int64_t N, int H, int K, void *out, int32_t *status, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -137,10 +161,11 @@ cudaError_t launch_combine(const void *Y, const int32_t *row_map, const float *w
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const uint4 *y = static_cast<const uint4 *>(Y);
+    const uint4 *res = static_cast<const uint4 *>(residual);
     uint4 *o = static_cast<uint4 *>(out);
     const int chunks = H / 8;
 #define MOE_COMBINE_LAUNCH(KK, C) \
-    return cudaLaunchKernelEx(&cfg, combine_kernel<KK, C>, y, row_map, w, N, H, K, o, status)
+    return cudaLaunchKernelEx(&cfg, combine_kernel<KK, C, RES>, y, row_map, w, N, H, K, res, o, status)
     switch (K) {
     case 1:
         switch (pow2_chunks_per_lane(chunks, 16)) {
@@ -171,6 +196,13 @@ cudaError_t launch_combine(const void *Y, const int32_t *row_map, const float *w
     default: MOE_COMBINE_LAUNCH(0, 1);
     }
 #undef MOE_COMBINE_LAUNCH
+}
+
+cudaError_t launch_combine(const void *Y, const int32_t *row_map, const float *w, const void *residual, int64_t N,
+                           int H, int K, void *out, int32_t *status, cudaStream_t stream)
+{
+    if (residual) return launch_combine_t<true>(Y, row_map, w, residual, N, H, K, out, status, stream);
+    return launch_combine_t<false>(Y, row_map, w, nullptr, N, H, K, out, status, stream);
 }
 
 }  // namespace moe

@@ -273,10 +273,21 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
     return r;
 }
 
+// Block-scale output: fp32 scales, or UE8M0 bytes (biased exponent, scale =
+// 2^(byte - 127)) -- the fp32 and e8m0 branches of the quantiser (PithTrain
+// page, §7.2 架构感知的量化核, _compute_fp8_scale).
+struct ScaleOut {
+    void *ptr;   // float [rows, H/128] or uint8 [rows, H/128]
+    int ue8m0;
+};
+
 // Quantise 8 bf16 values (one 16-byte chunk) held by each lane; lanes 0-15 and
 // 16-31 each hold one 128-element block.  Returns the 8 E4M3 codes and the
-// block's power-of-two scale s (x ~ q * s).
-__device__ __forceinline__ uint2 quant_chunk_e4m3(const uint4 &x, float &s_out)
+// block's power-of-two scale s (x ~ q * s).  Both branches take the same fp32
+// product t; the fp32 branch raises t to a power of two by its bit rule, the
+// e8m0 branch by the hardware round-toward-+inf conversion to UE8M0 (the same
+// value for every positive finite t).
+__device__ __forceinline__ uint2 quant_chunk_e4m3(const uint4 &x, float &s_out, int ue8m0)
 {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     float f[8];
@@ -292,8 +303,15 @@ __device__ __forceinline__ uint2 quant_chunk_e4m3(const uint4 &x, float &s_out)
     for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     // t = fl32(max(amax, 1e-4) * fl32(1/448)); s = t's exponent, bumped when t has a non-zero mantissa
     const float t = __fmul_rn(fmaxf(amax, 1e-4f), __uint_as_float(kRcp448Bits));
-    const uint32_t tb = __float_as_uint(t);
-    const uint32_t sbits = (tb & 0x7F800000u) + ((tb & 0x007FFFFFu) ? 0x00800000u : 0u);
+    uint32_t sbits;
+    if (ue8m0) {
+        uint16_t e;
+        asm("cvt.rp.satfinite.ue8m0x2.f32 %0, %1, %2;" : "=h"(e) : "f"(0.0f), "f"(t));
+        sbits = static_cast<uint32_t>(e & 0xFFu) << 23;
+    } else {
+        const uint32_t tb = __float_as_uint(t);
+        sbits = (tb & 0x7F800000u) + ((tb & 0x007FFFFFu) ? 0x00800000u : 0u);
+    }
     s_out = __uint_as_float(sbits);
     const float inv_s = __uint_as_float((254u - (sbits >> 23)) << 23);  // exact 1/s (a power of two)
     uint2 q;
@@ -320,11 +338,11 @@ __device__ __forceinline__ void load_row_batch(const uint4 *__restrict__ src, in
 
 template <bool kFp8, int CPL>
 __device__ __forceinline__ void quant_row_batch(const uint4 (&x)[CPL], uint2 (&q)[kFp8 ? CPL : 1],
-                                                float (&sc)[kFp8 ? CPL : 1])
+                                                float (&sc)[kFp8 ? CPL : 1], int ue8m0)
 {
     if constexpr (kFp8) {
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) q[j] = quant_chunk_e4m3(x[j], sc[j]);
+        for (int j = 0; j < CPL; ++j) q[j] = quant_chunk_e4m3(x[j], sc[j], ue8m0);
     }
 }
 
@@ -332,7 +350,7 @@ template <bool kBf16Out, bool kFp8, int CPL>
 __device__ __forceinline__ void store_row_batch(const uint4 (&x)[CPL], const uint2 (&q)[kFp8 ? CPL : 1],
                                                 const float (&sc)[kFp8 ? CPL : 1], int base, int my_row, int K,
                                                 int H, uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq,
-                                                float *__restrict__ Xs, int lane)
+                                                const ScaleOut Xs, int lane)
 {
     const int chunks = H >> 3;
     const int nb = H >> 7;
@@ -346,7 +364,13 @@ __device__ __forceinline__ void store_row_batch(const uint4 (&x)[CPL], const uin
             if constexpr (kBf16Out) __stcs(Xp + static_cast<int64_t>(r) * chunks + c, x[j]);
             if constexpr (kFp8) {
                 __stcs(reinterpret_cast<uint2 *>(Xq + static_cast<int64_t>(r) * H) + c, q[j]);
-                if ((lane & 15) == 0) Xs[static_cast<int64_t>(r) * nb + (c >> 4)] = sc[j];
+                if ((lane & 15) == 0) {
+                    const int64_t at = static_cast<int64_t>(r) * nb + (c >> 4);
+                    if (Xs.ue8m0)
+                        static_cast<uint8_t *>(Xs.ptr)[at] = static_cast<uint8_t>(__float_as_uint(sc[j]) >> 23);
+                    else
+                        static_cast<float *>(Xs.ptr)[at] = sc[j];
+                }
             }
         }
     }
@@ -360,7 +384,7 @@ __device__ __forceinline__ void store_row_batch(const uint4 (&x)[CPL], const uin
 template <bool kBf16Out, bool kFp8, int CPL>
 __device__ __forceinline__ void copy_token_rows(const uint4 *__restrict__ src, int my_row, int K, int H,
                                                 uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq,
-                                                float *__restrict__ Xs, int lane)
+                                                const ScaleOut Xs, int lane)
 {
     const int chunks = H >> 3;  // 16-byte chunks per row
     for (int base = 0; base < chunks; base += 32 * CPL) {
@@ -368,7 +392,7 @@ __device__ __forceinline__ void copy_token_rows(const uint4 *__restrict__ src, i
         uint2 q[kFp8 ? CPL : 1];
         float sc[kFp8 ? CPL : 1];
         load_row_batch<CPL>(src, base, chunks, lane, x);
-        quant_row_batch<kFp8, CPL>(x, q, sc);
+        quant_row_batch<kFp8, CPL>(x, q, sc, Xs.ue8m0);
         store_row_batch<kBf16Out, kFp8, CPL>(x, q, sc, base, my_row, K, H, Xp, Xq, Xs, lane);
     }
 }
@@ -376,7 +400,7 @@ __device__ __forceinline__ void copy_token_rows(const uint4 *__restrict__ src, i
 template <bool kBf16Out, bool kFp8, int CPL>
 __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(
     const uint4 *__restrict__ X, const int32_t *__restrict__ row_map, int64_t N, int H, int K,
-    uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq, float *__restrict__ Xs, int32_t *status)
+    uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq, const ScaleOut Xs, int32_t *status)
 {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -428,7 +452,7 @@ struct FusedParams {
     int32_t *counts, *offsets, *row_map, *src_slot;
     uint4 *Xp;
     uint8_t *Xq;
-    float *Xs;
+    ScaleOut Xs;
     int32_t *status;
     unsigned *bar;  // [0] arrive, [1] depart
     int32_t *hist;  // [gridDim.x][E]
@@ -503,7 +527,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
     float spre[kFp8 ? CPL : 1];
     if (pre) {
         load_row_batch<CPL>(p.X + (t0 + warp) * chunks, 0, chunks, lane, xpre);
-        quant_row_batch<kFp8, CPL>(xpre, qpre, spre);
+        quant_row_batch<kFp8, CPL>(xpre, qpre, spre, p.Xs.ue8m0);
     }
 
     // ---- stage the CTA's expert ids (0xFFFF: out of range)
@@ -718,7 +742,7 @@ cudaError_t launch_dispatch_meta(const int32_t *topk_idx, int64_t N, int E, int 
 }
 
 cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm,
-                           void *X_fp8, float *X_scale, int32_t *status, cudaStream_t stream)
+                           void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -739,11 +763,12 @@ cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int
     const uint4 *x = static_cast<const uint4 *>(X);
     uint4 *xp = static_cast<uint4 *>(X_perm);
     uint8_t *xq = static_cast<uint8_t *>(X_fp8);
+    const ScaleOut xs{X_scale, scale_ue8m0 ? 1 : 0};
     const int chunks = H / 8;
     int cpl = chunks > 256 ? 16 : chunks > 128 ? 8 : chunks > 64 ? 4 : chunks > 32 ? 2 : 1;
     if (X_fp8 && cpl > 8) cpl = 8;  // codes and scales stay live too
 #define MOE_PERMUTE_LAUNCH(B, F, C) \
-    return cudaLaunchKernelEx(&cfg, permute_kernel<B, F, C>, x, row_map, N, H, K, xp, xq, X_scale, status)
+    return cudaLaunchKernelEx(&cfg, permute_kernel<B, F, C>, x, row_map, N, H, K, xp, xq, xs, status)
 #define MOE_PERMUTE_CPL8(B, F)                         \
     switch (cpl) {                                     \
     case 1: MOE_PERMUTE_LAUNCH(B, F, 1);               \
@@ -815,7 +840,8 @@ cudaError_t launch_fused_cpl(const FusedParams &p, int grid, size_t smem, cudaSt
 
 cudaError_t launch_dispatch_fused(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
                                   int32_t *counts, int32_t *offsets, int32_t *row_map, int32_t *src_slot,
-                                  void *X_perm, void *X_fp8, float *X_scale, int32_t *status, void *workspace,
+                                  void *X_perm, void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status,
+                                  void *workspace,
                                   size_t workspace_bytes, cudaStream_t stream)
 {
     int dev = 0;
@@ -843,7 +869,7 @@ cudaError_t launch_dispatch_fused(const int32_t *topk_idx, const void *X, int64_
     p.src_slot = src_slot;
     p.Xp = static_cast<uint4 *>(X_perm);
     p.Xq = static_cast<uint8_t *>(X_fp8);
-    p.Xs = X_scale;
+    p.Xs = ScaleOut{X_scale, scale_ue8m0 ? 1 : 0};
     p.status = status;
     p.bar = static_cast<unsigned *>(workspace);
     p.hist = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + 256);

@@ -121,8 +121,9 @@ size_t moe_dispatch_workspace_size(int64_t N, int E, int K)
 }
 
 static moe_status validate_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K,
-                                   const void *X_perm, const void *X_fp8, const float *X_scale)
+                                   const void *X_perm, const void *X_fp8, const void *X_scale, int scale_format)
 {
+    if (scale_format != MOE_SCALE_FP32 && scale_format != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     if (!X || !row_map) return MOE_ERR_INVALID_ARG;
     if (!X_perm && !X_fp8) return MOE_ERR_INVALID_ARG;
     if ((X_fp8 == nullptr) != (X_scale == nullptr)) return MOE_ERR_INVALID_ARG;
@@ -130,21 +131,22 @@ static moe_status validate_permute(const void *X, const int32_t *row_map, int64_
     if (H % 8 != 0) return MOE_ERR_MISALIGNED;
     if (X_fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
     if (!aligned16(X) || (X_perm && !aligned16(X_perm)) || (X_fp8 && !aligned16(X_fp8)) ||
-        (X_scale && !aligned4(X_scale)) || !aligned4(row_map))
+        (X_scale && scale_format == MOE_SCALE_FP32 && !aligned4(X_scale)) || !aligned4(row_map))
         return MOE_ERR_MISALIGNED;
     (void)N;
     (void)K;
     return MOE_OK;
 }
 
-moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
-                        int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
-                        void *X_perm, void *X_fp8, float *X_scale, int32_t *status_word, void *workspace,
-                        size_t workspace_bytes, moe_stream_t stream)
+moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                           int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
+                           void *X_perm, void *X_fp8, void *X_scale, int scale_format, int32_t *status_word,
+                           void *workspace, size_t workspace_bytes, moe_stream_t stream)
 {
     moe_status st = check_topk(E, K);
     if (st != MOE_OK) return st;
     if ((st = check_rows(N, K)) != MOE_OK) return st;
+    if (scale_format != MOE_SCALE_FP32 && scale_format != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
     if (!aligned4(expert_counts) || !aligned4(expert_offsets) || (status_word && !aligned4(status_word)))
         return MOE_ERR_MISALIGNED;
@@ -157,8 +159,10 @@ moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H
         if (!topk_idx || !row_map) return MOE_ERR_INVALID_ARG;
         if (!aligned4(topk_idx) || !aligned4(row_map) || (src_slot && !aligned4(src_slot)))
             return MOE_ERR_MISALIGNED;
-        if (X && (st = validate_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale)) != MOE_OK) return st;
+        if (X && (st = validate_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, scale_format)) != MOE_OK)
+            return st;
     }
+    const int ue8m0 = scale_format == MOE_SCALE_UE8M0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (N == 0) {
         // no tokens: every count and offset is zero
@@ -168,8 +172,8 @@ moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H
     }
     if (use_ws) {
         const cudaError_t f = launch_dispatch_fused(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map,
-                                                    src_slot, X_perm, X_fp8, X_scale, status_word, workspace,
-                                                    workspace_bytes, s);
+                                                    src_slot, X_perm, X_fp8, X_scale, ue8m0, status_word,
+                                                    workspace, workspace_bytes, s);
         if (f == cudaSuccess) return MOE_OK;
         if (f != cudaErrorNotSupported) return MOE_ERR_CUDA;
     }
@@ -177,27 +181,43 @@ moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H
                                          status_word, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (X) {
-        e = launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, status_word, s);
+        e = launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, ue8m0, status_word, s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return MOE_OK;
 }
 
-moe_status moe_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm, void *X_fp8,
-                       float *X_scale, int32_t *status_word, moe_stream_t stream)
+moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                        int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
+                        void *X_perm, void *X_fp8, float *X_scale, int32_t *status_word, void *workspace,
+                        size_t workspace_bytes, moe_stream_t stream)
+{
+    return moe_dispatch_ex(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map, src_slot, X_perm, X_fp8,
+                           X_scale, MOE_SCALE_FP32, status_word, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_permute_ex(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm,
+                          void *X_fp8, void *X_scale, int scale_format, int32_t *status_word, moe_stream_t stream)
 {
     if (K < 1 || K > 16) return MOE_ERR_INVALID_ARG;
+    if (scale_format != MOE_SCALE_FP32 && scale_format != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     moe_status st = check_rows(N, K);
     if (st != MOE_OK) return st;
     if (N == 0) return MOE_OK;
-    if ((st = validate_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale)) != MOE_OK) return st;
+    if ((st = validate_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, scale_format)) != MOE_OK) return st;
     if (status_word && !aligned4(status_word)) return MOE_ERR_MISALIGNED;
-    return from_cuda(launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, status_word,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, scale_format == MOE_SCALE_UE8M0,
+                                    status_word, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_combine(const void *Y, const int32_t *row_map, const float *topk_w, int64_t N, int H, int K,
-                       void *out, int32_t *status_word, moe_stream_t stream)
+moe_status moe_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm, void *X_fp8,
+                       float *X_scale, int32_t *status_word, moe_stream_t stream)
+{
+    return moe_permute_ex(X, row_map, N, H, K, X_perm, X_fp8, X_scale, MOE_SCALE_FP32, status_word, stream);
+}
+
+static moe_status validate_combine(const void *Y, const int32_t *row_map, const float *topk_w, int64_t N, int H,
+                                   int K, const void *out, const int32_t *status_word)
 {
     if (K < 1 || K > 16) return MOE_ERR_INVALID_ARG;
     moe_status st = check_rows(N, K);
@@ -209,7 +229,26 @@ moe_status moe_combine(const void *Y, const int32_t *row_map, const float *topk_
     if (!aligned16(Y) || !aligned16(out) || !aligned4(row_map) || !aligned4(topk_w) ||
         (status_word && !aligned4(status_word)))
         return MOE_ERR_MISALIGNED;
-    return from_cuda(launch_combine(Y, row_map, topk_w, N, H, K, out, status_word,
+    return MOE_OK;
+}
+
+moe_status moe_combine(const void *Y, const int32_t *row_map, const float *topk_w, int64_t N, int H, int K,
+                       void *out, int32_t *status_word, moe_stream_t stream)
+{
+    const moe_status st = validate_combine(Y, row_map, topk_w, N, H, K, out, status_word);
+    if (st != MOE_OK || N == 0) return st;
+    return from_cuda(launch_combine(Y, row_map, topk_w, nullptr, N, H, K, out, status_word,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_residual(const void *Y, const int32_t *row_map, const float *topk_w, const void *residual,
+                                int64_t N, int H, int K, void *out, int32_t *status_word, moe_stream_t stream)
+{
+    const moe_status st = validate_combine(Y, row_map, topk_w, N, H, K, out, status_word);
+    if (st != MOE_OK || N == 0) return st;
+    if (!residual) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(residual)) return MOE_ERR_MISALIGNED;
+    return from_cuda(launch_combine(Y, row_map, topk_w, residual, N, H, K, out, status_word,
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 

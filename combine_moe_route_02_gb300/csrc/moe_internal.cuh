@@ -294,15 +294,17 @@ cudaError_t launch_dispatch_meta(const int32_t *topk_idx, int64_t N, int E, int 
 // cluster metadata kernel + launch_permute).
 cudaError_t launch_dispatch_fused(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
                                   int32_t *counts, int32_t *offsets, int32_t *row_map, int32_t *src_slot,
-                                  void *X_perm, void *X_fp8, float *X_scale, int32_t *status, void *workspace,
-                                  size_t workspace_bytes, cudaStream_t stream);
+                                  void *X_perm, void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status,
+                                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t fused_workspace_bytes(int E);
 
+// X_scale: fp32 [N*K, H/128], or (scale_ue8m0 != 0) one UE8M0 byte per block.
 cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm,
-                           void *X_fp8, float *X_scale, int32_t *status, cudaStream_t stream);
+                           void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status, cudaStream_t stream);
 
-cudaError_t launch_combine(const void *Y, const int32_t *row_map, const float *w, int64_t N, int H, int K,
-                           void *out, int32_t *status, cudaStream_t stream);
+// residual: NULL for the plain weighted combine.
+cudaError_t launch_combine(const void *Y, const int32_t *row_map, const float *w, const void *residual, int64_t N,
+                           int H, int K, void *out, int32_t *status, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count(int device);

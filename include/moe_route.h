@@ -56,6 +56,12 @@ typedef enum moe_status {
     MOE_ERR_BAD_INDEX = 7      /* (status_word only) topk_idx entry outside [0,E) */
 } moe_status;
 
+/* Format of the E4M3 block scales (moe_dispatch_ex, moe_permute_ex). */
+typedef enum moe_scale_format {
+    MOE_SCALE_FP32 = 0,        /* fp32 [N*K, H/128]: the power-of-two scale s itself */
+    MOE_SCALE_UE8M0 = 1        /* uint8 [N*K, H/128]: UE8M0 byte b, s = 2^(b - 127) */
+} moe_scale_format;
+
 /* Router implementation selector for moe_route_ex. */
 typedef enum moe_route_algo {
     MOE_ROUTE_AUTO = 0,        /* tensor-core kernel where the shape allows it */
@@ -140,6 +146,29 @@ MOE_API moe_status moe_dispatch(const int32_t *topk_idx, const void *X,
                         moe_stream_t stream);
 
 /*
+ * moe_dispatch_ex -- moe_dispatch with a choice of block-scale format for the
+ * E4M3 copy.  The PithTrain page (§7.2 架构感知的量化核, _compute_fp8_scale)
+ * gives two branches of the scale rule: fp32 scales (the bit rule quoted at
+ * moe_permute below) and, on Blackwell, E8M0 scales -- the same fp32 product
+ * t = fl32(max(amax, 1e-4) * fl32(1/448)) converted with round-toward-+inf to
+ * an unsigned 8-bit exponent (cvt.rp.satfinite.ue8m0x2.f32).  Both give the
+ * same power-of-two s and hence the same E4M3 codes; MOE_SCALE_UE8M0 stores
+ * one byte b per block (s = 2^(b - 127)) instead of a float.
+ *   X_scale      fp32 [N*K, H/128] (MOE_SCALE_FP32, 4-byte aligned) or
+ *                uint8 [N*K, H/128] (MOE_SCALE_UE8M0), with X_fp8; or NULL
+ *   scale_format a moe_scale_format; anything else is MOE_ERR_INVALID_ARG
+ * Every other argument, and the errors, as moe_dispatch.
+ */
+MOE_API moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X,
+                           int64_t N, int H, int E, int K,
+                           int32_t *expert_counts, int32_t *expert_offsets,
+                           int32_t *row_map, int32_t *src_slot,
+                           void *X_perm, void *X_fp8, void *X_scale, int scale_format,
+                           int32_t *status_word,
+                           void *workspace, size_t workspace_bytes,
+                           moe_stream_t stream);
+
+/*
  * moe_dispatch_noalloc -- moe_dispatch without a caller-provided workspace.
  * The pages have no counterpart: this is a convenience of this library for
  * callers that cannot allocate device memory when they dispatch -- engines that
@@ -185,6 +214,12 @@ MOE_API moe_status moe_permute(const void *X, const int32_t *row_map,
                        void *X_perm, void *X_fp8, float *X_scale,
                        int32_t *status_word, moe_stream_t stream);
 
+/* moe_permute with a choice of block-scale format (see moe_dispatch_ex). */
+MOE_API moe_status moe_permute_ex(const void *X, const int32_t *row_map,
+                          int64_t N, int H, int K,
+                          void *X_perm, void *X_fp8, void *X_scale, int scale_format,
+                          int32_t *status_word, moe_stream_t stream);
+
 /*
  * moe_combine -- weighted gather back to token order.
  * The weighted part of forward_aggregate on the PithTrain page (§6.1
@@ -199,6 +234,22 @@ MOE_API moe_status moe_permute(const void *X, const int32_t *row_map,
 MOE_API moe_status moe_combine(const void *Y, const int32_t *row_map, const float *topk_w,
                        int64_t N, int H, int K, void *out,
                        int32_t *status_word, moe_stream_t stream);
+
+/*
+ * moe_combine_residual -- moe_combine plus the residual connection: the whole
+ * of forward_aggregate on the PithTrain page (§6.1 模型协议先行, "weighted
+ * expert output + residual connection"), fused into the same pass:
+ *   out[n,:] = sum_{k=0}^{K-1} topk_w[n,k] * Y[row_map[n*K+k], :] + residual[n,:]
+ * with the weighted sum accumulated in fp32 in k order, the residual added in
+ * fp32, and one rounding to bf16 (nearest even).
+ * Arguments: as moe_combine, plus residual bf16 [N,H] (required, 16-byte
+ * aligned).  out may be the residual buffer itself (in-place update of the
+ * residual stream); any other overlap of out with Y or residual is undefined.
+ * Errors: as moe_combine; a NULL residual with N > 0 is MOE_ERR_INVALID_ARG.
+ */
+MOE_API moe_status moe_combine_residual(const void *Y, const int32_t *row_map, const float *topk_w,
+                                const void *residual, int64_t N, int H, int K, void *out,
+                                int32_t *status_word, moe_stream_t stream);
 
 /* A static, human-readable name for a status code. */
 MOE_API const char *moe_status_string(moe_status status);

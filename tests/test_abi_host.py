@@ -114,6 +114,17 @@ def test_permute_and_combine_validation(L):
     assert L.moe_combine(A, A2, A3, 8, 64, 17, A4, None, None) == INVALID
     assert L.moe_combine(A, A2, A3, 8, 60, 2, A4, None, None) == MISALIGNED
     assert L.moe_combine(A, A2, A3, 8, 64, 2, A4 + 8, None, None) == MISALIGNED
+    # block-scale format: fp32 scales need 4-byte alignment, UE8M0 bytes none; other formats are refused
+    assert L.moe_permute_ex(A, A2, 8, 128, 2, A3, A4, A + 2, 0, None, None) == MISALIGNED
+    assert L.moe_permute_ex(A, A2, 8, 128, 2, A3, A4, A, 2, None, None) == INVALID
+    assert L.moe_permute_ex(A, A2, 0, 128, 2, A3, A4, A, 7, None, None) == INVALID
+    assert L.moe_dispatch_ex(A, A2, 8, 128, 16, 2, A3, A4, A, A2, A3, A4, A, 5, None, None, 0, None) == INVALID
+    R = 0x50000
+    assert L.moe_combine_residual(A, A2, A3, R, 0, 64, 2, A4, None, None) == OK
+    assert L.moe_combine_residual(A, A2, A3, None, 8, 64, 2, A4, None, None) == INVALID
+    assert L.moe_combine_residual(A, A2, A3, R + 8, 8, 64, 2, A4, None, None) == MISALIGNED
+    assert L.moe_combine_residual(None, A2, A3, R, 8, 64, 2, A4, None, None) == INVALID
+    assert L.moe_combine_residual(A, A2, A3, R, 8, 64, 0, A4, None, None) == INVALID
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
@@ -121,6 +132,9 @@ def test_valid_call_without_gpu_fails_loudly(L):
     # arguments pass validation, then the first CUDA call fails: MOE_ERR_CUDA, no crash
     assert route(L) == CUDA
     assert L.moe_combine(A, A2, A3, 8, 64, 2, A4, None, None) == CUDA
+    assert L.moe_combine_residual(A, A2, A3, 0x50000, 8, 64, 2, A4, None, None) == CUDA
+    # UE8M0 scale bytes need no alignment: the call passes validation (then fails on CUDA)
+    assert L.moe_permute_ex(A, A2, 8, 128, 2, A3, A4, A + 2, 1, None, None) == CUDA
 
 
 def test_binding_refuses_cpu_tensors():

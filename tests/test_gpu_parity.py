@@ -252,6 +252,52 @@ def test_dispatch_workspace_reused_many_times():
     assert int(ws[:8].abs().sum()) == 0
 
 
+@pytest.mark.parametrize("N,H,K", [(1, 128, 1), (100, 128, 8), (257, 384, 2), (64, 4096, 4), (300, 2048, 8),
+                                   (7, 256, 16)])
+def test_permute_ue8m0_scales_match_oracle(N, H, K):
+    E = max(K, 16)
+    X = mi.random_bf16((N, H), seed=N + 2 * H, scale=2.0)
+    if N >= 3:
+        X[0, :128] = 0.0
+        X[1, :128] *= 1e-6
+        X[2, :] *= 1e3
+    idx = mi.random_topk_idx(N, E, K, seed=N + 3 * K)
+    _, _, row_map, _ = oracle.dispatch(idx.numpy(), E)
+    rm = torch.from_numpy(row_map).to(DEV)
+    st = status_word()
+    Xp, Xq, Xs = moe.permute(X.to(DEV), rm, K, bf16=True, fp8=True, scale_format="ue8m0", status=st)
+    _, Xq32, Xs32 = moe.permute(X.to(DEV), rm, K, bf16=False, fp8=True)
+    torch.cuda.synchronize()
+    assert st.item() == 0 and Xs.dtype == torch.uint8
+    rXq, rXs = oracle.permute_ue8m0(bits(X), row_map, K)
+    assert np.array_equal(Xq.cpu().numpy(), rXq)
+    assert np.array_equal(Xs.cpu().numpy(), rXs)
+    assert np.array_equal(bits(Xp), oracle.permute(bits(X), row_map, K))
+    # the two branches agree on the GPU too: same codes, byte = exponent field of the fp32 scale
+    assert torch.equal(Xq, Xq32)
+    assert torch.equal(Xs.to(torch.int32), (Xs32.view(torch.int32) >> 23) & 0xFF)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("N,H,E,K,bf16", [(300, 2048, 64, 8, True), (20000, 256, 128, 8, False),
+                                          (513, 1024, 16, 2, True)])
+def test_dispatch_ue8m0_scales_match_oracle(N, H, E, K, bf16, fused):
+    X = mi.random_bf16((N, H), seed=N + H, scale=4.0)
+    idx = mi.random_topk_idx(N, E, K, seed=N + K)
+    st = status_word()
+    d = moe.dispatch(idx.to(DEV), E, X.to(DEV), fp8=True, bf16=bf16, fused=fused, status=st,
+                     scale_format="ue8m0")
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    c, o, r, s = oracle.dispatch(idx.numpy(), E)
+    assert np.array_equal(d.row_map.cpu().numpy(), r)
+    rXq, rXs = oracle.permute_ue8m0(bits(X), r, K)
+    assert np.array_equal(d.X_fp8.cpu().numpy(), rXq)
+    assert np.array_equal(d.X_scale.cpu().numpy(), rXs)
+    if bf16:
+        assert np.array_equal(bits(d.X_perm), oracle.permute(bits(X), r, K))
+
+
 def test_permute_fp8_only():
     N, H, K = 200, 512, 2
     X = mi.random_bf16((N, H), seed=5)
@@ -285,6 +331,48 @@ def test_combine_matches_oracle(N, H, K):
     Yd = oracle.bf16_bits_to_f64_array(bits(Y))[row_map.reshape(N, K)]
     mag = np.einsum("nk,nkh->nh", np.abs(w.numpy().astype(np.float64)), np.abs(Yd))
     combine_close(bits(out), ref, extra_atol=2.0**-20 * mag)
+
+
+@pytest.mark.parametrize("N,H,K", [(1, 8, 1), (77, 136, 3), (300, 1024, 2), (129, 2048, 8), (50, 4096, 2),
+                                   (64, 256, 16), (200, 512, 4), (33, 40, 5)])
+def test_combine_residual_matches_oracle(N, H, K):
+    E = max(K, 8)
+    Y = mi.random_bf16((N * K, H), seed=N + 3 * H)
+    R = mi.random_bf16((N, H), seed=N + 5 * H, scale=2.0)
+    w = mi.random_weights(N, K, seed=N + K)
+    idx = mi.random_topk_idx(N, E, K, seed=N + 7)
+    _, _, row_map, _ = oracle.dispatch(idx.numpy(), E)
+    ref = oracle.combine_residual(bits(Y), row_map, w.numpy(), bits(R))
+    st = status_word()
+    out = moe.combine(Y.to(DEV), torch.from_numpy(row_map).to(DEV), w.to(DEV), residual=R.to(DEV), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    # signed terms can cancel: allow the fp32 accumulation error of the terms
+    Yd = oracle.bf16_bits_to_f64_array(bits(Y))[row_map.reshape(N, K)]
+    mag = np.einsum("nk,nkh->nh", np.abs(w.numpy().astype(np.float64)), np.abs(Yd)) + \
+        np.abs(oracle.bf16_bits_to_f64_array(bits(R)))
+    combine_close(bits(out), ref, extra_atol=2.0**-20 * mag)
+
+
+def test_combine_residual_in_place():
+    # out is the residual buffer: the residual stream is updated in place
+    N, H, K, E = 500, 1024, 4, 16
+    Y = mi.random_bf16((N * K, H), seed=41)
+    R = mi.random_bf16((N, H), seed=42)
+    w = mi.random_weights(N, K, seed=43)
+    idx = mi.random_topk_idx(N, E, K, seed=44)
+    _, _, row_map, _ = oracle.dispatch(idx.numpy(), E)
+    rm = torch.from_numpy(row_map).to(DEV)
+    Rg = R.to(DEV)
+    sep = moe.combine(Y.to(DEV), rm, w.to(DEV), residual=Rg)
+    moe.combine(Y.to(DEV), rm, w.to(DEV), residual=Rg, out=Rg)
+    torch.cuda.synchronize()
+    assert torch.equal(Rg.view(torch.int16), sep.view(torch.int16))
+    # zero weights: the residual comes back bit for bit
+    again = moe.combine(Y.to(DEV), rm, torch.zeros_like(w).to(DEV), residual=R.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(again), bits(R)) or np.array_equal(
+        bits(again)[bits(R) != 0x8000], bits(R)[bits(R) != 0x8000])
 
 
 def test_combine_bad_row_reports_status():
