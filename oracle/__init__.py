@@ -68,6 +68,8 @@ def _load():
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_f64_to_e4m3_satfinite.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_e4m3_satfinite.restype = ctypes.c_uint8
+        lib.oracle_logsumexp.argtypes = [P, I64, I64, P]
+        lib.oracle_load_stats.argtypes = [P, I64, P, I64, ctypes.c_double, P]
         lib.oracle_ue8m0_block_scale.argtypes = [ctypes.c_double]
         lib.oracle_ue8m0_block_scale.restype = ctypes.c_uint8
         lib.oracle_permute_ue8m0.argtypes = [P, P, I64, I64, I64, P, P]
@@ -127,6 +129,27 @@ def route(X_bits, W_bits, bias=None, K=1, renorm=True, want_logits=False, want_p
     if want_probs:
         out.append(probs)
     return tuple(out)
+
+
+def logsumexp(logits):
+    """Per-token log-sum-exp of fp64 logits [N,E] (NaN as -inf): fp64 [N]."""
+    lib = _load()
+    L = _c(logits, np.float64)
+    N, E = L.shape
+    out = np.empty(N, np.float64)
+    _check(lib.oracle_logsumexp(_ptr(L), N, E, _ptr(out)), "oracle_logsumexp")
+    return out
+
+
+def load_stats(counts, lse=None, z_coef=1e-3):
+    """Expert-load statistics: (max/mean, p95/mean, z_loss, mean) as fp64."""
+    lib = _load()
+    c = _c(counts, np.int32)
+    l = None if lse is None else _c(lse, np.float64)
+    out = np.empty(4, np.float64)
+    _check(lib.oracle_load_stats(_ptr(c), c.shape[0], _ptr(l), 0 if l is None else l.shape[0],
+                                 float(z_coef), _ptr(out)), "oracle_load_stats")
+    return out
 
 
 def dispatch(topk_idx, E):

@@ -17,6 +17,8 @@
  *   [moe-engine]  "moe-engine：面向万卡集群的稀疏MoE训练基础设施" (zingnex.cn),
  *                 section 融合Triton路由内核: tokens @ gate_w -> softmax ->
  *                 top-K -> renorm; K-round selection sort;
+ *                 section 专家负载均衡: imbalance max/mean, 95th percentile,
+ *                 z-loss regularisation with weight 1e-3;
  *                 section 实验结果与性能数据 / Token守恒验证:
  *                 sum(dispatch_cnt) == N*K.
  *   [PithTrain]   "一万行Python构建MoE训练栈：解构4D并行、DualPipeV调度与FP8算子"
@@ -317,6 +319,93 @@ int oracle_route(const uint16_t *X, const uint16_t *W, const float *bias,
         free(chosen);
     }
     return failed ? ORACLE_NO_MEM : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Router statistics  ([moe-engine] 专家负载均衡)                       */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Per-token log-sum-exp of the router logits, the quantity a z-loss squares:
+ * lse[n] = log( sum_e exp(L[n,e]) ), computed as m + log(sum_e exp(L[n,e] - m))
+ * with m = max_e L[n,e], in fp64.  NaN logits count as -inf (as in the
+ * selection); a token whose logits are all -inf gets -inf.
+ * logits fp64 [N,E] (the logits_out of oracle_route), lse fp64 [N].
+ */
+int oracle_logsumexp(const double *logits, int64_t N, int64_t E, double *lse)
+{
+    if (N < 0 || E <= 0)
+        return ORACLE_BAD_ARG;
+    for (int64_t n = 0; n < N; ++n) {
+        double m = -INFINITY;
+        for (int64_t e = 0; e < E; ++e) {
+            double x = logits[n * E + e];
+            if (!isnan(x) && x > m)
+                m = x;
+        }
+        if (m == -INFINITY) {
+            lse[n] = -INFINITY;
+            continue;
+        }
+        double z = 0.0;
+        for (int64_t e = 0; e < E; ++e) {
+            double x = logits[n * E + e];
+            if (!isnan(x))
+                z += exp(x - m);
+        }
+        lse[n] = m + log(z);
+    }
+    return ORACLE_OK;
+}
+
+static int cmp_int32(const void *a, const void *b)
+{
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * Expert-load statistics of the moe-engine page (section 专家负载均衡): the
+ * imbalance ratio max/mean of the per-expert slot counts, the 95th percentile
+ * of the counts over the mean, and the z-loss with weight coef:
+ *   stats[0] = max_e counts[e] / mean,    mean = sum_e counts[e] / E
+ *   stats[1] = P95(counts) / mean, P95 by linear interpolation between the
+ *              sorted counts at position 0.95 * (E - 1)
+ *   stats[2] = coef * (1/N) * sum_n lse[n]^2      (0 when lse is NULL or N == 0)
+ *   stats[3] = mean
+ * The ratios are 0 when no slot was counted.  All in fp64.
+ */
+int oracle_load_stats(const int32_t *counts, int64_t E, const double *lse, int64_t N,
+                      double coef, double *stats)
+{
+    if (E <= 0 || N < 0)
+        return ORACLE_BAD_ARG;
+    int32_t *sorted = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    if (!sorted)
+        return ORACLE_NO_MEM;
+    double total = 0.0, mx = 0.0;
+    for (int64_t e = 0; e < E; ++e) {
+        sorted[e] = counts[e];
+        total += counts[e];
+        if (counts[e] > mx)
+            mx = counts[e];
+    }
+    qsort(sorted, (size_t)E, sizeof(int32_t), cmp_int32);
+    double pos = 0.95 * (double)(E - 1);
+    int64_t lo = (int64_t)floor(pos);
+    int64_t hi = lo + 1 < E ? lo + 1 : E - 1;
+    double p95 = sorted[lo] + (pos - (double)lo) * (double)(sorted[hi] - sorted[lo]);
+    free(sorted);
+    double mean = total / (double)E;
+    stats[0] = mean > 0.0 ? mx / mean : 0.0;
+    stats[1] = mean > 0.0 ? p95 / mean : 0.0;
+    double zsum = 0.0;
+    if (lse)
+        for (int64_t n = 0; n < N; ++n)
+            zsum += lse[n] * lse[n];
+    stats[2] = (lse && N > 0) ? coef * zsum / (double)N : 0.0;
+    stats[3] = mean;
+    return ORACLE_OK;
 }
 
 /* ------------------------------------------------------------------ */

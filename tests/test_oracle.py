@@ -149,6 +149,52 @@ def test_permute_ue8m0_matches_fp32_scale_path():
     assert np.array_equal(np.ldexp(1.0, Xs8.astype(np.int32) - 127), Xs.astype(np.float64))
 
 
+# ---------------------------------------------------------------- router statistics
+
+def test_logsumexp_matches_scipy_and_special_cases():
+    from scipy.special import logsumexp as sp_lse
+    X, W, bias = mi.make_route_inputs(64, 128, 32, seed=11, skew=True)
+    _, _, L = oracle.route(mi.bf16_bits(X), mi.bf16_bits(W), bias.numpy(), 2, want_logits=True)
+    lse = oracle.logsumexp(L)
+    assert np.allclose(lse, sp_lse(L, axis=1), rtol=0, atol=1e-12)
+    # equal logits: c + log(E); one expert: the logit itself; NaN counts as -inf; all -inf gives -inf
+    E = 16
+    Lc = np.full((3, E), 2.5)
+    Lc[1, :] = -7.0
+    Lc[2, 3] = np.nan
+    Lc[2, 4:] = -np.inf
+    got = oracle.logsumexp(Lc)
+    assert got[0] == pytest.approx(2.5 + math.log(E), abs=1e-15)
+    assert got[1] == pytest.approx(-7.0 + math.log(E), abs=1e-15)
+    assert got[2] == pytest.approx(2.5 + math.log(3), abs=1e-15)
+    assert oracle.logsumexp(np.array([[1.25]]))[0] == 1.25
+    assert oracle.logsumexp(np.full((1, 4), -np.inf))[0] == -np.inf
+
+
+def test_load_stats_hand_example():
+    # counts 1,2,3,4: mean 2.5, max/mean 1.6; p95 at position 2.85 -> 3 + 0.85 = 3.85 -> 1.54
+    st = oracle.load_stats(np.array([3, 1, 4, 2], np.int32), np.array([1.0, -2.0, 3.0]), 1e-3)
+    assert st[0] == pytest.approx(1.6, abs=1e-15)
+    assert st[1] == pytest.approx(3.85 / 2.5, abs=1e-15)
+    assert st[2] == pytest.approx(1e-3 * (1 + 4 + 9) / 3, abs=1e-18)
+    assert st[3] == 2.5
+    # no lse: no z-loss; all counts zero: ratios 0; a uniform load: ratios 1
+    assert oracle.load_stats(np.zeros(8, np.int32))[0:3].tolist() == [0.0, 0.0, 0.0]
+    assert oracle.load_stats(np.full(8, 5, np.int32))[0:2].tolist() == [1.0, 1.0]
+
+
+def test_load_stats_matches_numpy_percentile():
+    rng = np.random.default_rng(12)
+    for E in (1, 2, 7, 64, 256):
+        c = rng.integers(0, 1000, E).astype(np.int32)
+        lse = rng.normal(size=50)
+        st = oracle.load_stats(c, lse, 1e-3)
+        mean = c.sum() / E
+        assert st[0] == pytest.approx(c.max() / mean, rel=1e-14)
+        assert st[1] == pytest.approx(np.percentile(c, 95) / mean, rel=1e-14)
+        assert st[2] == pytest.approx(1e-3 * np.mean(lse ** 2), rel=1e-14)
+
+
 # ---------------------------------------------------------------- route
 
 def test_route_golden_ties():
