@@ -43,7 +43,7 @@ ABI_VERSION = 1
 EXPORTED_SYMBOLS = (
     "moe_route", "moe_route_ex", "moe_dispatch_workspace_size", "moe_dispatch",
     "moe_permute", "moe_combine", "moe_status_string", "moe_abi_version", "moe_dispatch_noalloc",
-    "moe_combine_residual", "moe_dispatch_ex", "moe_permute_ex",
+    "moe_combine_residual", "moe_dispatch_ex", "moe_permute_ex", "moe_route_stats", "moe_load_stats",
 )
 
 SCALE_FP32, SCALE_UE8M0 = 0, 1
@@ -98,6 +98,10 @@ def lib():
     L.moe_combine.restype = I32
     L.moe_combine_residual.argtypes = [P, P, P, P, I64, I32, I32, P, P, P]
     L.moe_combine_residual.restype = I32
+    L.moe_route_stats.argtypes = [P, P, P, I64, I32, I32, I32, I32, P, P, P, P, P, I32, P]
+    L.moe_route_stats.restype = I32
+    L.moe_load_stats.argtypes = [P, I32, P, I64, ctypes.c_float, P, P]
+    L.moe_load_stats.restype = I32
     L.moe_dispatch_ex.argtypes = [P, P, I64, I32, I32, I32, P, P, P, P, P, P, P, I32, P, P, SZ, P]
     L.moe_dispatch_ex.restype = I32
     L.moe_permute_ex.argtypes = [P, P, I64, I32, I32, P, P, P, I32, P, P]
@@ -168,6 +172,46 @@ def route(X: torch.Tensor, W_gate: torch.Tensor, K: int, bias: Optional[torch.Te
                               _ptr(topk_idx), _ptr(topk_w), _ptr(status), _ALGOS[algo], _stream(stream))
     _check(code, "moe_route")
     return topk_idx, topk_w
+
+
+def route_stats(X: torch.Tensor, W_gate: torch.Tensor, K: int, bias: Optional[torch.Tensor] = None,
+                renorm: bool = True, algo: str = "auto", want_lse: bool = True, want_counts: bool = True,
+                status=None, stream=None):
+    """Fused router with its statistics: returns (topk_idx, topk_w, lse fp32 [N] or None,
+    expert_counts int32 [E] or None)."""
+    N, H = X.shape
+    E = W_gate.shape[1]
+    _need(X, "X", torch.bfloat16)
+    _need(W_gate, "W_gate", torch.bfloat16, (H, E))
+    if bias is not None:
+        _need(bias, "bias", torch.float32, (E,))
+    dev = X.device
+    topk_idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    topk_w = torch.empty((N, K), dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if want_counts else None
+    code = lib().moe_route_stats(_ptr(X), _ptr(W_gate), _ptr(bias), N, H, E, K, int(bool(renorm)),
+                                 _ptr(topk_idx), _ptr(topk_w), _ptr(lse), _ptr(counts), _ptr(status),
+                                 _ALGOS[algo], _stream(stream))
+    _check(code, "moe_route_stats")
+    return topk_idx, topk_w, lse, counts
+
+
+def load_stats(expert_counts: torch.Tensor, lse: Optional[torch.Tensor] = None, z_coef: float = 1e-3,
+               out=None, stream=None) -> torch.Tensor:
+    """Expert-load statistics: fp32 [4] = (max/mean, p95/mean, z_loss, mean)."""
+    _need(expert_counts, "expert_counts", torch.int32)
+    E = expert_counts.shape[0]
+    N = 0
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+        N = lse.shape[0]
+    if out is None:
+        out = torch.empty(4, dtype=torch.float32, device=expert_counts.device)
+    _need(out, "stats", torch.float32, (4,))
+    code = lib().moe_load_stats(_ptr(expert_counts), E, _ptr(lse), N, float(z_coef), _ptr(out), _stream(stream))
+    _check(code, "moe_load_stats")
+    return out
 
 
 @dataclass

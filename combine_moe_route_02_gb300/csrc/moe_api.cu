@@ -105,6 +105,52 @@ moe_status moe_route_ex(const void *X, const void *W_gate, const float *bias, in
     return from_cuda(launch_route_tc(a, s));
 }
 
+moe_status moe_route_stats(const void *X, const void *W_gate, const float *bias, int64_t N, int H, int E, int K,
+                           int renorm, int32_t *topk_idx, float *topk_w, float *lse, int32_t *expert_counts,
+                           int32_t *status_word, int algo, moe_stream_t stream)
+{
+    moe_status st = check_topk(E, K);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(N, K)) != MOE_OK) return st;
+    if (algo < MOE_ROUTE_AUTO || algo > MOE_ROUTE_SIMT) return MOE_ERR_INVALID_ARG;
+    if (H < 1) return MOE_ERR_INVALID_ARG;
+    if ((lse && !aligned4(lse)) || (expert_counts && !aligned4(expert_counts))) return MOE_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        if (expert_counts && cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (!X || !W_gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_MISALIGNED;
+    if (!aligned16(X) || !aligned16(W_gate) || !aligned4(topk_idx) || !aligned4(topk_w) ||
+        (bias && !aligned4(bias)) || (status_word && !aligned4(status_word)))
+        return MOE_ERR_MISALIGNED;
+
+    RouteArgs a{X, W_gate, bias, N, H, E, K, renorm ? 1 : 0, topk_idx, topk_w, status_word};
+    a.lse = lse;
+    a.counts = expert_counts;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    const bool tc_ok = route_tc_supported(a, dev);
+    if (algo == MOE_ROUTE_TCGEN05 && !tc_ok) return MOE_ERR_UNSUPPORTED;
+    // the kernels add their selections to the counts
+    if (expert_counts && cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (algo == MOE_ROUTE_SIMT || !tc_ok) return from_cuda(launch_route_simt(a, s));
+    return from_cuda(launch_route_tc(a, s));
+}
+
+moe_status moe_load_stats(const int32_t *expert_counts, int E, const float *lse, int64_t N, float z_coef,
+                          float *stats, moe_stream_t stream)
+{
+    if (E < 1 || E > 256 || N < 0) return MOE_ERR_INVALID_ARG;
+    if (!expert_counts || !stats) return MOE_ERR_INVALID_ARG;
+    if (!aligned4(expert_counts) || !aligned4(stats) || (lse && !aligned4(lse))) return MOE_ERR_MISALIGNED;
+    return from_cuda(launch_load_stats(expert_counts, E, lse, N, z_coef, stats,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_route(const void *X, const void *W_gate, const float *bias, int64_t N, int H, int E, int K,
                      int renorm, int32_t *topk_idx, float *topk_w, int32_t *status_word, moe_stream_t stream)
 {

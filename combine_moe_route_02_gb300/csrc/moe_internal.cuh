@@ -278,12 +278,18 @@ struct RouteArgs {
     int32_t *topk_idx;
     float *topk_w;
     int32_t *status;
+    float *lse = nullptr;        // [N] per-token logsumexp of the logits, or nullptr
+    int32_t *counts = nullptr;   // [E] selections per expert, accumulated (zeroed first), or nullptr
 };
 
 // Whether the tensor-core router can take this shape on the current device.
 bool route_tc_supported(const RouteArgs &a, int device);
 cudaError_t launch_route_tc(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_route_simt(const RouteArgs &a, cudaStream_t stream);
+
+// Expert-load statistics (one CTA): stats[0..3] = max/mean, p95/mean, z-loss, mean.
+cudaError_t launch_load_stats(const int32_t *counts, int E, const float *lse, int64_t N, float z_coef,
+                              float *stats, cudaStream_t stream);
 
 cudaError_t launch_dispatch_meta(const int32_t *topk_idx, int64_t N, int E, int K, int32_t *counts,
                                  int32_t *offsets, int32_t *row_map, int32_t *src_slot, int32_t *status,

@@ -32,7 +32,8 @@ __device__ __forceinline__ bool ranks_above(float v, int i, float bv, int bi)
 
 __global__ void __launch_bounds__(kSimtWarps * 32) route_simt_kernel(
     const uint16_t *__restrict__ X, const uint16_t *__restrict__ W, const float *__restrict__ bias, int64_t N,
-    int H, int E, int K, int renorm, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w)
+    int H, int E, int K, int renorm, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+    float *__restrict__ lse, int32_t *__restrict__ counts)
 {
     __shared__ float logits_s[kSimtWarps][kMaxE];
     const int warp = threadIdx.x >> 5;
@@ -119,18 +120,21 @@ __global__ void __launch_bounds__(kSimtWarps * 32) route_simt_kernel(
             }
         }
         float denom = sum_sel;
-        if (!renorm) {
+        if (!renorm || lse) {
+            // the full softmax denominator: sum over all experts of exp(logit - max)
             float z = 0.f;
 #pragma unroll
             for (int i = 0; i < kPerLane; ++i)
-                if (lane + 32 * i < E) z += expf(mine[i] - first_v);
+                if (lane + 32 * i < E && mine[i] != -INFINITY) z += expf(mine[i] - first_v);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-            denom = z;
+            if (!renorm) denom = z;
+            if (lse && lane == 0) lse[n] = first_v == -INFINITY ? -INFINITY : first_v + logf(z);
         }
         if (lane < K) {
             topk_idx[n * K + lane] = my_i;
             topk_w[n * K + lane] = my_v / denom;
+            if (counts && my_i >= 0 && my_i < E) atomicAdd(counts + my_i, 1);
         }
         __syncwarp();
     }
@@ -149,7 +153,7 @@ cudaError_t launch_route_simt(const RouteArgs &a, cudaStream_t stream)
     const int grid = static_cast<int>(blocks_needed < int64_t(sms) * 8 ? blocks_needed : int64_t(sms) * 8);
     route_simt_kernel<<<grid, kSimtWarps * 32, 0, stream>>>(
         static_cast<const uint16_t *>(a.X), static_cast<const uint16_t *>(a.W), a.bias, a.N, a.H, a.E, a.K,
-        a.renorm, a.topk_idx, a.topk_w);
+        a.renorm, a.topk_idx, a.topk_w, a.lse, a.counts);
     return cudaGetLastError();
 }
 

@@ -73,7 +73,10 @@ struct TcParams {
     int32_t *topk_idx;
     float *topk_w;
     int32_t *status;
+    float *lse;            // [N] per-token logsumexp of the logits, or nullptr
+    int32_t *counts;       // [E] slot count per expert (accumulated; zeroed by the caller), or nullptr
     int N, H, E, K, renorm;
+    int need_z;            // the full softmax denominator is needed (renorm off, or lse requested)
     int EP, NP, stages, nsplit, kb_per, tiles;
     uint32_t tmem_cols;
     uint32_t exch_off;     // byte offset of the epilogue exchange area (from the aligned base)
@@ -218,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
     unsigned char *b_base = smem + static_cast<size_t>(p.stages) * kABytes;
     TcSmemTail &tail = *reinterpret_cast<TcSmemTail *>(smem + p.tail_off);
     float *bias_s = reinterpret_cast<float *>(&tail + 1);
+    int *hist_s = reinterpret_cast<int *>(bias_s + p.EP);                // [EP] selections per expert
     // exchange area, token-minor so that the lanes of a warp touch consecutive words
     int *lst_k = reinterpret_cast<int *>(smem + p.exch_off);            // [2 halves][KMAX][128] keys
     int *lst_i = lst_k + 2 * kBM * KMAX;                                   // [2 halves][KMAX][128] ids
@@ -272,8 +276,10 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
     pdl_wait_prior_grids();
     if (warp != 0) {
         // the producer starts streaming at once; the bias is needed by the epilogue only
-        for (int e = threadIdx.x - 32; e < p.EP; e += kThreads - 32)
+        for (int e = threadIdx.x - 32; e < p.EP; e += kThreads - 32) {
             bias_s[e] = (p.bias != nullptr && e < E) ? p.bias[e] : 0.f;
+            hist_s[e] = 0;
+        }
         named_barrier_sync(5, kThreads - 32);
     }
 
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                         const float x1 = logit_of(v[t + 1], bias_s[c + t + 1]);
                         topk_push<KMAX>(ak, ai, order_key(x0), c + t);
                         topk_push<KMAX>(bk, bi, order_key(x1), c + t + 1);
-                        if (!p.renorm) {
+                        if (p.need_z) {
                             online_sumexp(x0, r, z);
                             online_sumexp(x1, r, z);
                         }
@@ -405,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                         const float x1 = logit_of(v[t + 1], bias_s[c + t + 1]);
                         topk_push<KMAX>(ak, ai, order_key(x0), c + t);
                         topk_push<KMAX>(bk, bi, order_key(x1), c + t + 1);
-                        if (!p.renorm) {
+                        if (p.need_z) {
                             online_sumexp(x0, r, z);
                             online_sumexp(x1, r, z);
                         }
@@ -444,24 +450,32 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                         const int ib = pb < K ? oi[pb * kBM] : kEmpty;
                         const bool take_b = ranks_above(kb, ib, ka, ia);
                         wrow[k * kBM] = key_value(take_b ? kb : ka);
-                        if (n < p.N) p.topk_idx[static_cast<int64_t>(n) * K + k] = take_b ? ib : ia;
+                        const int sel = take_b ? ib : ia;
+                        if (n < p.N) {
+                            p.topk_idx[static_cast<int64_t>(n) * K + k] = sel;
+                            if (p.counts && sel < E) atomicAdd(hist_s + sel, 1);
+                        }
                         pa += take_b ? 0 : 1;
                         pb += take_b ? 1 : 0;
                     }
-                    const float m = wrow[0];
-                    float denom = 0.f;
-                    if (p.renorm) {
-#pragma unroll 1
-                        for (int k = 0; k < K; ++k) denom += expf(wrow[k * kBM] - m);
-                    } else {
+                    const float m = wrow[0];   // the largest logit
+                    float zfull = 0.f;         // sum over all experts of exp(logit - m)
+                    if (p.need_z) {
                         const float r0 = lst_rz[row], z0 = lst_rz[kBM + row];
                         const float r1 = lst_rz[2 * kBM + row], z1 = lst_rz[3 * kBM + row];
-                        denom = (z0 > 0.f ? z0 * expf(r0 - m) : 0.f) + (z1 > 0.f ? z1 * expf(r1 - m) : 0.f);
+                        zfull = (z0 > 0.f ? z0 * expf(r0 - m) : 0.f) + (z1 > 0.f ? z1 * expf(r1 - m) : 0.f);
+                    }
+                    float denom = zfull;
+                    if (p.renorm) {
+                        denom = 0.f;
+#pragma unroll 1
+                        for (int k = 0; k < K; ++k) denom += expf(wrow[k * kBM] - m);
                     }
                     if (n < p.N) {
 #pragma unroll 1
                         for (int k = 0; k < K; ++k)
                             p.topk_w[static_cast<int64_t>(n) * K + k] = expf(wrow[k * kBM] - m) / denom;
+                        if (p.lse) p.lse[n] = m == -INFINITY ? -INFINITY : m + logf(zfull);
                     }
                 }
                 named_barrier_sync(1 + q, 64);   // the lists have been consumed
@@ -549,11 +563,14 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                 topk_pop_if<KMAX>(bk, bi, bi[0] == i);
                 if (part == 0) {
                     wrow[k * kBM] = fv;
-                    if (n < p.N) p.topk_idx[static_cast<int64_t>(n) * K + k] = i;
+                    if (n < p.N) {
+                        p.topk_idx[static_cast<int64_t>(n) * K + k] = i;
+                        if (p.counts && i < E) atomicAdd(hist_s + i, 1);
+                    }
                 }
             }
             float z = 0.f;
-            if (!p.renorm) {
+            if (p.need_z) {
 #pragma unroll 1
                 for (int col = part; col < E; col += G) {
                     float x = 0.f;
@@ -576,11 +593,17 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
 #pragma unroll 1
                 for (int k = 0; k < K; ++k)
                     p.topk_w[static_cast<int64_t>(n) * K + k] = expf(wrow[k * kBM] - m) / denom;
+                if (p.lse) p.lse[n] = m == -INFINITY ? -INFINITY : m + logf(z);
             }
         }
     }
 
     __syncthreads();
+    if (p.counts) {
+        // this CTA's selections per expert, added to the grid-wide counts
+        for (int e = threadIdx.x; e < E; e += kThreads)
+            if (hist_s[e] != 0) atomicAdd(p.counts + e, hist_s[e]);
+    }
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, p.tmem_cols);
@@ -645,7 +668,7 @@ bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, TcLayout &L)
     const size_t slot = kABytes + static_cast<size_t>(EP) * kBK * 2;
     const size_t staging = split ? static_cast<size_t>(kBM) * stage_row_floats(NP) * sizeof(float) : 0;
     const size_t exch = (split ? 0 : exch_lists_bytes(kmax)) + win_bytes(kmax);
-    const size_t fixed = 1024 + staging + exch + sizeof(TcSmemTail) + sizeof(float) * EP;
+    const size_t fixed = 1024 + staging + exch + sizeof(TcSmemTail) + (sizeof(float) + sizeof(int)) * EP;
     const int max_st = split ? (kb_per < kMaxStages ? (kb_per < 1 ? 1 : kb_per) : kMaxStages) : kMaxStages;
     const int min_st = split ? 1 : 2;
     const size_t budgets[2] = {split ? static_cast<size_t>(113 * 1024) : kSmemLimit, kSmemLimit};
@@ -718,11 +741,14 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     q.topk_idx = a.topk_idx;
     q.topk_w = a.topk_w;
     q.status = a.status;
+    q.lse = a.lse;
+    q.counts = a.counts;
     q.N = static_cast<int>(a.N);
     q.H = a.H;
     q.E = a.E;
     q.K = a.K;
     q.renorm = a.renorm;
+    q.need_z = (!a.renorm || a.lse != nullptr) ? 1 : 0;
     q.EP = (a.E + 63) / 64 * 64;
     q.NP = (a.E + 15) / 16 * 16;
     q.tiles = static_cast<int>((a.N + kBM - 1) / kBM);

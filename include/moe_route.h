@@ -102,6 +102,41 @@ MOE_API moe_status moe_route_ex(const void *X, const void *W_gate, const float *
                         int32_t *topk_idx, float *topk_w, int32_t *status_word,
                         int algo, moe_stream_t stream);
 
+/*
+ * moe_route_stats -- moe_route_ex with the router statistics of the
+ * moe-engine page (section 专家负载均衡) taken in the same pass:
+ *   lse[n]           = log(sum_e exp(L[n,e]))   fp32 [N] or NULL: the per-token
+ *                      logsumexp a z-loss squares (-inf for a token whose
+ *                      logits are all -inf or NaN)
+ *   expert_counts[e] = #{(n,k) : topk_idx[n,k] == e}   int32 [E] or NULL:
+ *                      the expert histogram, counted in the router's epilogue
+ *                      (the same values moe_dispatch writes)
+ * expert_counts is overwritten (set to zero on `stream`, then accumulated by
+ * the kernel).  Other arguments, layout and errors as moe_route_ex.
+ */
+MOE_API moe_status moe_route_stats(const void *X, const void *W_gate, const float *bias,
+                           int64_t N, int H, int E, int K, int renorm,
+                           int32_t *topk_idx, float *topk_w, float *lse,
+                           int32_t *expert_counts, int32_t *status_word,
+                           int algo, moe_stream_t stream);
+
+/*
+ * moe_load_stats -- expert-load statistics from the counts (and optionally the
+ * logsumexp values) of moe_route_stats, in one small kernel:
+ *   stats[0] = max_e counts[e] / mean              (imbalance ratio)
+ *   stats[1] = P95(counts) / mean, P95 by linear interpolation between the
+ *              sorted counts at position 0.95 * (E - 1)
+ *   stats[2] = z_coef * (1/N) * sum_n lse[n]^2      (0 if lse is NULL or N == 0)
+ *   stats[3] = mean = sum_e counts[e] / E
+ * The ratios are 0 when every count is 0.  The sums are taken in fp64 in a
+ * fixed order (deterministic).  counts int32 [E] (1 <= E <= 256), lse fp32 [N]
+ * or NULL, stats fp32 [4] (all device memory).
+ * Errors: MOE_ERR_INVALID_ARG (NULL counts or stats, E out of range, N < 0),
+ * MOE_ERR_MISALIGNED, MOE_ERR_CUDA.
+ */
+MOE_API moe_status moe_load_stats(const int32_t *expert_counts, int E, const float *lse, int64_t N,
+                          float z_coef, float *stats, moe_stream_t stream);
+
 /* Bytes of device workspace moe_dispatch needs for these sizes (0 means the
  * workspace pointer may be NULL). */
 MOE_API size_t moe_dispatch_workspace_size(int64_t N, int E, int K);

@@ -119,6 +119,14 @@ def test_permute_and_combine_validation(L):
     assert L.moe_permute_ex(A, A2, 8, 128, 2, A3, A4, A, 2, None, None) == INVALID
     assert L.moe_permute_ex(A, A2, 0, 128, 2, A3, A4, A, 7, None, None) == INVALID
     assert L.moe_dispatch_ex(A, A2, 8, 128, 16, 2, A3, A4, A, A2, A3, A4, A, 5, None, None, 0, None) == INVALID
+    # router statistics: argument checks before any CUDA call
+    assert L.moe_route_stats(A, A2, None, 16, 64, 16, 2, 1, A3, A4, A + 2, None, None, 0, None) == MISALIGNED
+    assert L.moe_route_stats(A, A2, None, 16, 64, 16, 17, 1, A3, A4, None, None, None, 0, None) == INVALID
+    assert L.moe_route_stats(A, A2, None, 16, 64, 16, 2, 1, A3, A4, None, None, None, 9, None) == INVALID
+    assert L.moe_load_stats(A, 0, None, 0, ctypes.c_float(1e-3), A2, None) == INVALID
+    assert L.moe_load_stats(A, 257, None, 0, ctypes.c_float(1e-3), A2, None) == INVALID
+    assert L.moe_load_stats(None, 16, None, 0, ctypes.c_float(1e-3), A2, None) == INVALID
+    assert L.moe_load_stats(A, 16, None, 0, ctypes.c_float(1e-3), A2 + 2, None) == MISALIGNED
     R = 0x50000
     assert L.moe_combine_residual(A, A2, A3, R, 0, 64, 2, A4, None, None) == OK
     assert L.moe_combine_residual(A, A2, A3, None, 8, 64, 2, A4, None, None) == INVALID
@@ -133,6 +141,7 @@ def test_valid_call_without_gpu_fails_loudly(L):
     assert route(L) == CUDA
     assert L.moe_combine(A, A2, A3, 8, 64, 2, A4, None, None) == CUDA
     assert L.moe_combine_residual(A, A2, A3, 0x50000, 8, 64, 2, A4, None, None) == CUDA
+    assert L.moe_load_stats(A, 16, None, 0, ctypes.c_float(1e-3), A2, None) == CUDA
     # UE8M0 scale bytes need no alignment: the call passes validation (then fails on CUDA)
     assert L.moe_permute_ex(A, A2, 8, 128, 2, A3, A4, A + 2, 1, None, None) == CUDA
 

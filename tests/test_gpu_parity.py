@@ -126,6 +126,51 @@ def test_route_nan_logit_is_minus_inf(algo):
     assert np.all(gi[:, -1] == 3) and np.array_equal(gi, oi)
 
 
+@pytest.mark.parametrize("algo", ["tcgen05", "simt"])
+@pytest.mark.parametrize("N,H,E,K,renorm,skew", [(7, 64, 16, 2, True, False), (300, 1024, 64, 4, True, False),
+                                                 (2048, 1024, 64, 2, True, False), (257, 512, 128, 8, False, False),
+                                                 (20000, 128, 256, 16, True, False), (40000, 256, 64, 2, True, True),
+                                                 (4096, 2048, 64, 4, False, True)])
+def test_route_stats_match_oracle(algo, N, H, E, K, renorm, skew):
+    X, W, bias = mi.make_route_inputs(N, H, E, seed=N + K, skew=skew)
+    st = status_word()
+    Xd, Wd = X.to(DEV), W.to(DEV)
+    bd = None if bias is None else bias.to(DEV)
+    idx, w, lse, counts = moe.route_stats(Xd, Wd, K, bd, renorm, algo, status=st)
+    idx0, w0 = moe.route(Xd, Wd, K, bd, renorm, algo)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    # the statistics change nothing else
+    assert torch.equal(idx, idx0) and torch.equal(w, w0)
+    ref_idx, ref_w, L, P = oracle_route(X, W, bias, K, renorm)
+    compare_topk(idx.cpu().numpy(), w.cpu().numpy(), ref_idx, ref_w, L, P, renorm=renorm)
+    # counts: exactly the histogram of the selected experts
+    assert np.array_equal(counts.cpu().numpy(), np.bincount(idx.cpu().numpy().ravel(), minlength=E))
+    # lse: fp32 logits accumulated over H, then exp/log in fp32
+    ref_lse = oracle.logsumexp(L)
+    got = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref_lse) <= 5e-5 + 2e-6 * np.abs(ref_lse)), np.max(np.abs(got - ref_lse))
+
+
+def test_load_stats_match_oracle():
+    for seed, (N, H, E, K, skew) in enumerate([(512, 256, 32, 2, False), (16384, 2048, 128, 8, False),
+                                               (65536, 1024, 64, 2, True), (100, 64, 1, 1, False),
+                                               (3000, 128, 256, 16, False)]):
+        X, W, bias = mi.make_route_inputs(N, H, E, seed=seed, skew=skew)
+        idx, w, lse, counts = moe.route_stats(X.to(DEV), W.to(DEV), K, None if bias is None else bias.to(DEV))
+        stats = moe.load_stats(counts, lse, 1e-3)
+        torch.cuda.synchronize()
+        c = counts.cpu().numpy()
+        assert int(c.sum()) == N * K
+        ref = oracle.load_stats(c, lse.cpu().numpy().astype(np.float64), 1e-3)
+        got = stats.cpu().numpy().astype(np.float64)
+        assert np.allclose(got, ref, rtol=1e-6, atol=0), (got, ref)
+    # no logsumexp: the z-loss is 0
+    z = moe.load_stats(counts)
+    torch.cuda.synchronize()
+    assert float(z[2]) == 0.0
+
+
 def test_route_empty_is_noop():
     X = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
     W = torch.zeros(64, 16, dtype=torch.bfloat16, device=DEV)
