@@ -68,6 +68,7 @@ def _load():
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_f64_to_e4m3_satfinite.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_e4m3_satfinite.restype = ctypes.c_uint8
+        lib.oracle_dispatch_ep.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_logsumexp.argtypes = [P, I64, I64, P]
         lib.oracle_load_stats.argtypes = [P, I64, P, I64, ctypes.c_double, P]
         lib.oracle_ue8m0_block_scale.argtypes = [ctypes.c_double]
@@ -164,6 +165,28 @@ def dispatch(topk_idx, E):
     _check(lib.oracle_dispatch(_ptr(idx), N, E, K, _ptr(counts), _ptr(offsets),
                                _ptr(row_map), _ptr(src_slot)), "oracle_dispatch")
     return counts, offsets, row_map, src_slot
+
+
+def dispatch_ep(topk_idx, E, ep_size):
+    """Expert-parallel dispatch metadata with dedup: returns a dict of counts, offsets,
+    row_map, src_slot, rank_counts, rank_offsets, send_token (rank_offsets[-1] rows),
+    slot_send_row, expand_idx, send_meta [R, P+1]."""
+    lib = _load()
+    idx = _c(topk_idx, np.int32)
+    N, K = idx.shape
+    R = ep_size
+    P = E // R if R > 0 else 0
+    out = dict(counts=np.empty(E, np.int32), offsets=np.empty(E + 1, np.int32),
+               row_map=np.empty(N * K, np.int32), src_slot=np.empty(N * K, np.int32),
+               rank_counts=np.empty(R, np.int32), rank_offsets=np.empty(R + 1, np.int32),
+               send_token=np.empty(max(N * min(K, R), 1), np.int32),
+               slot_send_row=np.empty(N * K, np.int32), expand_idx=np.empty(N * K, np.int32),
+               send_meta=np.empty((R, P + 1), np.int32))
+    _check(lib.oracle_dispatch_ep(_ptr(idx), N, E, K, R, *(_ptr(out[k]) for k in (
+        "counts", "offsets", "row_map", "src_slot", "rank_counts", "rank_offsets", "send_token",
+        "slot_send_row", "expand_idx", "send_meta"))), "oracle_dispatch_ep")
+    out["send_token"] = out["send_token"][:out["rank_offsets"][-1]]
+    return out
 
 
 def permute(X_bits, row_map, K, fp8=False):

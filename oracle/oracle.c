@@ -474,6 +474,76 @@ int oracle_dispatch(const int32_t *topk_idx, int64_t N, int64_t E, int64_t K,
 }
 
 /*
+ * Expert-parallel dispatch metadata with token deduplication ([PithTrain]
+ * §8.2, fused_dedup_prepare_dispatch: per-expert and per-EP-rank counts,
+ * prefix sums, send metadata, dedup scatter, counting sort and expand_idx),
+ * for the tokens of one GPU.  Experts are split over R = ep_size ranks,
+ * P = E / R consecutive experts each: rank(e) = e / P.  A token goes to a
+ * rank once however many of its K experts live there (deduplication).
+ *   rank_counts[r]   = #{n : some k has rank(topk[n,k]) == r}
+ *   rank_offsets[r]  = sum_{r' < r} rank_counts[r'],  rank_offsets[R] = total rows
+ *   send_token[row]  = the token of send row `row`; rows are ordered by
+ *                      (rank, token): rank-contiguous, tokens ascending
+ *   slot_send_row[s] = the send row carrying the token of slot s to the rank
+ *                      of its expert
+ *   expand_idx[row]  = for row `row` of the expert-contiguous order of
+ *                      oracle_dispatch (slot s = its src_slot), the index of
+ *                      s's token within its rank's block of send rows:
+ *                      slot_send_row[s] - rank_offsets[rank(topk[s])]
+ *   send_meta[r*(P+1)]         = rank_counts[r]
+ *   send_meta[r*(P+1) + 1 + j] = counts[r*P + j]   (the per-rank metadata
+ *                      exchanged before the token all-to-all, dedup count first)
+ * counts / offsets / row_map / src_slot as in oracle_dispatch.  send_token is
+ * sized for N * min(K, R) rows.  Returns ORACLE_BAD_ARG unless E % R == 0.
+ */
+int oracle_dispatch_ep(const int32_t *topk_idx, int64_t N, int64_t E, int64_t K, int64_t R,
+                       int32_t *counts, int32_t *offsets, int32_t *row_map, int32_t *src_slot,
+                       int32_t *rank_counts, int32_t *rank_offsets, int32_t *send_token,
+                       int32_t *slot_send_row, int32_t *expand_idx, int32_t *send_meta)
+{
+    if (N < 0 || E <= 0 || K <= 0 || R <= 0 || E % R != 0)
+        return ORACLE_BAD_ARG;
+    int st = oracle_dispatch(topk_idx, N, E, K, counts, offsets, row_map, src_slot);
+    if (st != ORACLE_OK)
+        return st;
+    int64_t P = E / R;
+    /* row of (rank r, token n), -1 if the token has no expert on r */
+    int32_t *row_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R * (N > 0 ? N : 1)));
+    if (!row_of)
+        return ORACLE_NO_MEM;
+    int32_t row = 0;
+    for (int64_t r = 0; r < R; ++r) {
+        rank_offsets[r] = row;
+        for (int64_t n = 0; n < N; ++n) {
+            int hit = 0;
+            for (int64_t k = 0; k < K; ++k)
+                if (topk_idx[n * K + k] / P == r)
+                    hit = 1;
+            row_of[r * N + n] = hit ? row : -1;
+            if (hit)
+                send_token[row++] = (int32_t)n;
+        }
+        rank_counts[r] = row - rank_offsets[r];
+    }
+    rank_offsets[R] = row;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            slot_send_row[n * K + k] = row_of[(topk_idx[n * K + k] / P) * N + n];
+    for (int64_t q = 0; q < N * K; ++q) {
+        int64_t s = src_slot[q];
+        int64_t r = topk_idx[s] / P;
+        expand_idx[q] = slot_send_row[s] - rank_offsets[r];
+    }
+    for (int64_t r = 0; r < R; ++r) {
+        send_meta[r * (P + 1)] = rank_counts[r];
+        for (int64_t j = 0; j < P; ++j)
+            send_meta[r * (P + 1) + 1 + j] = counts[r * P + j];
+    }
+    free(row_of);
+    return ORACLE_OK;
+}
+
+/*
  * Xp[row_map[n*K+k], :] = X[n, :]   (bf16 bits copied)
  * If Xq/Xs are given (H % 128 == 0), every 1x128 block b of X[n,:] also
  * gives s = oracle_fp8_block_scale(max |x|) and q = E4M3(x / s); both are

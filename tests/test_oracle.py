@@ -149,6 +149,58 @@ def test_permute_ue8m0_matches_fp32_scale_path():
     assert np.array_equal(np.ldexp(1.0, Xs8.astype(np.int32) - 127), Xs.astype(np.float64))
 
 
+# ---------------------------------------------------------------- expert-parallel dispatch metadata
+
+def brute_force_ep(idx, E, R):
+    """Plain-Python statement of the dedup'd send layout: rows are the sorted set of (rank, token)."""
+    N, K = idx.shape
+    P = E // R
+    pairs = sorted({(int(e) // P, n) for n in range(N) for e in idx[n]})
+    row = {pr: i for i, pr in enumerate(pairs)}
+    rank_counts = [sum(1 for r, _ in pairs if r == q) for q in range(R)]
+    rank_offsets = [0] + list(itertools.accumulate(rank_counts))
+    send_token = [n for _, n in pairs]
+    slot_send_row = [row[(int(idx[n, k]) // P, n)] for n in range(N) for k in range(K)]
+    return rank_counts, rank_offsets, send_token, slot_send_row
+
+
+@pytest.mark.parametrize("N,E,K,R", [(1, 4, 1, 2), (9, 8, 3, 4), (20, 16, 4, 4), (33, 12, 5, 3), (50, 64, 8, 8),
+                                     (17, 6, 2, 6), (25, 10, 4, 1)])
+def test_dispatch_ep_matches_brute_force(N, E, K, R):
+    idx = mi.random_topk_idx(N, E, K, seed=N * E + R).numpy()
+    o = oracle.dispatch_ep(idx, E, R)
+    rc, ro, st, ssr = brute_force_ep(idx, E, R)
+    assert o["rank_counts"].tolist() == rc and o["rank_offsets"].tolist() == ro
+    assert o["send_token"].tolist() == st and o["slot_send_row"].tolist() == ssr
+    P = E // R
+    counts = np.bincount(idx.ravel(), minlength=E)
+    assert np.array_equal(o["send_meta"][:, 0], rc)
+    assert np.array_equal(o["send_meta"][:, 1:].ravel(), counts)
+    # expanding a rank's received rows by expand_idx gives, row by row, the token of every
+    # expert-ordered slot of that rank
+    for q in range(N * K):
+        s = o["src_slot"][q]
+        r = idx.ravel()[s] // P
+        assert 0 <= o["expand_idx"][q] < rc[r]
+        assert st[ro[r] + o["expand_idx"][q]] == s // K
+
+
+def test_dispatch_ep_special_cases():
+    N, E, K = 40, 16, 4
+    idx = mi.random_topk_idx(N, E, K, seed=5).numpy()
+    # one rank: every token once, in order; each slot's row is its token
+    o = oracle.dispatch_ep(idx, E, 1)
+    assert o["rank_counts"].tolist() == [N] and o["send_token"].tolist() == list(range(N))
+    assert np.array_equal(o["slot_send_row"], np.arange(N * K) // K)
+    assert np.array_equal(o["expand_idx"], o["src_slot"] // K)
+    # one expert per rank: nothing to deduplicate (the K experts of a token are distinct),
+    # so the rank order is the expert order
+    o = oracle.dispatch_ep(idx, E, E)
+    assert np.array_equal(o["slot_send_row"], o["row_map"])
+    assert np.array_equal(o["rank_counts"], o["counts"])
+    assert np.array_equal(o["expand_idx"], np.arange(N * K) - np.repeat(o["offsets"][:-1], o["counts"]))
+
+
 # ---------------------------------------------------------------- router statistics
 
 def test_logsumexp_matches_scipy_and_special_cases():
