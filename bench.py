@@ -28,6 +28,8 @@ import statistics
 import subprocess
 import sys
 import threading
+
+import numpy as np
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -54,6 +56,8 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--scale-format", default="fp32", choices=["fp32", "ue8m0"],
                    help="E4M3 block-scale output of fp8 workloads: fp32 scales or UE8M0 exponent bytes")
+    p.add_argument("--ep-size", type=int, default=0,
+                   help="dispatch as moe_dispatch_ep with this many EP ranks (dedup'd send rows, expand_idx)")
     p.add_argument("--residual", action="store_true",
                    help="combine with the residual connection (forward_aggregate: moe_combine_residual)")
     return p.parse_args()
@@ -124,7 +128,7 @@ def measured_peaks():
 
 # ----------------------------------------------------------------- algorithmic bytes per launch
 
-def kernel_bytes(w: mi.Workload, residual: bool = False, ue8m0: bool = False):
+def kernel_bytes(w: mi.Workload, residual: bool = False, ue8m0: bool = False, ep_rows=None):
     N, H, E, K = w.N, w.H, w.E, w.K
     route = N * 2 * H + H * E * 2 + N * K * 8 + (E * 4 if w.skew else 0)
     meta = N * K * 4 * 3                      # read topk_idx, write row_map and src_slot
@@ -134,6 +138,11 @@ def kernel_bytes(w: mi.Workload, residual: bool = False, ue8m0: bool = False):
     combine = N * K * 2 * H + N * 2 * H + N * K * 8
     if residual:
         combine += N * 2 * H                  # read the residual row
+    if ep_rows is not None:
+        # EP dispatch: read topk_idx, write row_map, slot_send_row, expand_idx and
+        # send_token, read X once and write one row per (token, rank)
+        return {"route": route, "dispatch": N * K * 4 * 4 + ep_rows * 4 + N * 2 * H + ep_rows * 2 * H,
+                "combine": combine}
     return {"route": route, "dispatch": meta + permute, "combine": combine}
 
 
@@ -201,16 +210,22 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- CPU oracle baseline
 
-def oracle_pass(oracle, Xb, Wb, bias, w: mi.Workload, Y, R=None, ue8m0=False):
+def oracle_pass(oracle, Xb, Wb, bias, w: mi.Workload, Y, R=None, ue8m0=False, ep_size=0):
     """One pass of the oracle over the workload: route, dispatch, permute, combine
-    (with the residual R when given; UE8M0 block scales when ue8m0)."""
+    (with the residual R when given; UE8M0 block scales when ue8m0; the EP
+    metadata and dedup'd send rows when ep_size)."""
     idx, tw = oracle.route(Xb, Wb, bias, w.K, w.renorm)
-    counts, offsets, row_map, src_slot = oracle.dispatch(idx, w.E)
-    if w.fp8 and ue8m0:
-        oracle.permute(Xb, row_map, w.K)
-        oracle.permute_ue8m0(Xb, row_map, w.K)
+    if ep_size:
+        ep = oracle.dispatch_ep(idx, w.E, ep_size)
+        row_map = ep["row_map"]
+        np.take(Xb, ep["send_token"], axis=0)      # the dedup'd send rows (a library gather)
     else:
-        oracle.permute(Xb, row_map, w.K, fp8=w.fp8)
+        counts, offsets, row_map, src_slot = oracle.dispatch(idx, w.E)
+        if w.fp8 and ue8m0:
+            oracle.permute(Xb, row_map, w.K)
+            oracle.permute_ue8m0(Xb, row_map, w.K)
+        else:
+            oracle.permute(Xb, row_map, w.K, fp8=w.fp8)
     if R is None:
         oracle.combine(Y, row_map, tw)
     else:
@@ -224,7 +239,7 @@ def residual_rows(w: mi.Workload, rank: int = 0):
 
 
 def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000, residual: bool = False,
-                 ue8m0: bool = False):
+                 ue8m0: bool = False, ep_size: int = 0):
     import oracle
     X, W, bias = mi.make_workload_inputs(w)
     Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
@@ -234,7 +249,7 @@ def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000, residual:
     R = mi.bf16_bits(residual_rows(w)) if residual else None
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, ep_size)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= max_reps:
@@ -256,10 +271,10 @@ def run_reference(args, rank, world):
     R = mi.bf16_bits(residual_rows(w)) if args.residual else None
     ue8m0 = args.scale_format == "ue8m0"
     for _ in range(args.warmup):
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, args.ep_size)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, args.ep_size)
     el = time.perf_counter() - t0
     value = args.steps * w.N / el
     sample = f"the whole {w.name} workload ({w.N} tokens) per step, fp64 C oracle"
@@ -274,8 +289,9 @@ def run_reference(args, rank, world):
 
 
 def combine_config(args):
-    c = {"combine": "forward_aggregate: weighted sum + residual, one bf16 rounding" if args.residual
-         else "weighted sum"}
+    c = {"dispatch": f"moe_dispatch_ep, ep_size {args.ep_size}"} if args.ep_size else {}
+    c["combine"] = ("forward_aggregate: weighted sum + residual, one bf16 rounding" if args.residual
+                    else "weighted sum")
     if mi.WORKLOADS[args.workload].fp8:
         c["fp8_scales"] = args.scale_format
     return c
@@ -284,7 +300,6 @@ def combine_config(args):
 # ----------------------------------------------------------------- the GPU arm
 
 def run_ours(args, rank, world, local):
-    import numpy as np
     import torch
 
     import combine_moe_route_02_gb300 as moe
@@ -327,8 +342,19 @@ def run_ours(args, rank, world, local):
     sp = ctypes.c_void_p(stream.cuda_stream)
     route_args = (vp(Xd), vp(Wd), vp(bd), N, H, E, K, int(w.renorm), vp(idx), vp(tw), vp(st), moe.ROUTE_AUTO, sp)
     fmt = moe.SCALE_UE8M0 if args.scale_format == "ue8m0" else moe.SCALE_FP32
+    disp_fn = L.moe_dispatch_ex
     disp_args = (vp(idx), vp(Xd), N, H, E, K, vp(d.expert_counts), vp(d.expert_offsets), vp(d.row_map),
                  vp(d.src_slot), vp(d.X_perm), vp(d.X_fp8), vp(d.X_scale), fmt, vp(st), vp(ws), ws.numel(), sp)
+    ep_rows = None
+    if args.ep_size:
+        de = moe.dispatch_ep(idx, E, args.ep_size, Xd)
+        torch.cuda.synchronize()
+        ep_rows = int(de.rank_offsets[-1])
+        disp_fn = L.moe_dispatch_ep
+        disp_args = (vp(idx), vp(Xd), N, H, E, K, args.ep_size, vp(de.expert_counts), vp(de.expert_offsets),
+                     vp(de.row_map), vp(de.rank_counts), vp(de.rank_offsets), vp(de.send_token),
+                     vp(de.slot_send_row), vp(de.expand_idx), vp(de.send_meta), vp(de.X_send), vp(st), vp(ws),
+                     ws.numel(), sp)
     if R is None:
         comb_fn = L.moe_combine
         comb_args = (vp(Y), vp(d.row_map), vp(tw), N, H, K, vp(out), vp(st), sp)
@@ -343,7 +369,7 @@ def run_ours(args, rank, world, local):
         rc |= L.moe_route_ex(*route_args)
         if ev is not None:
             ev[1].record(stream)
-        rc |= L.moe_dispatch_ex(*disp_args)        # counting sort + row permute (+ E4M3), one launch
+        rc |= disp_fn(*disp_args)                  # counting sort + row permute (+ E4M3), one launch
         if ev is not None:
             ev[2].record(stream)
         rc |= comb_fn(*comb_args)
@@ -352,7 +378,7 @@ def run_ours(args, rank, world, local):
         if rc:
             raise RuntimeError(f"a library call failed: {moe.status_string(rc)}")
 
-    kernels_per_step = 3
+    kernels_per_step = 5 if args.ep_size else 3   # moe_dispatch_ep is three launches
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         step()
@@ -413,11 +439,11 @@ def run_ours(args, rank, world, local):
         gs.wait_stream(stream)
         with torch.cuda.stream(gs):
             for _ in range(2):  # warm the graph stream's workspace and plans
-                L.moe_route_ex(*g_route); L.moe_dispatch_ex(*g_disp); comb_fn(*g_comb)
+                L.moe_route_ex(*g_route); disp_fn(*g_disp); comb_fn(*g_comb)
         torch.cuda.synchronize()
         cg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg, stream=gs):
-            rc = L.moe_route_ex(*g_route) | L.moe_dispatch_ex(*g_disp) | comb_fn(*g_comb)
+            rc = L.moe_route_ex(*g_route) | disp_fn(*g_disp) | comb_fn(*g_comb)
         if rc:
             raise RuntimeError(moe.status_string(rc))
         gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ksteps)]
@@ -458,7 +484,7 @@ def run_ours(args, rank, world, local):
         return
 
     peak, peak_src = measured_peaks()
-    kb = kernel_bytes(w, args.residual, args.scale_format == "ue8m0")
+    kb = kernel_bytes(w, args.residual, args.scale_format == "ue8m0", ep_rows)
     kern = {}
     for n in names:
         ms = statistics.fmean(per[n])
@@ -490,7 +516,7 @@ def run_ours(args, rank, world, local):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, residual=args.residual,
-                                            ue8m0=args.scale_format == "ue8m0")
+                                            ue8m0=args.scale_format == "ue8m0", ep_size=args.ep_size)
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()

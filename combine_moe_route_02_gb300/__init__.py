@@ -44,6 +44,7 @@ EXPORTED_SYMBOLS = (
     "moe_route", "moe_route_ex", "moe_dispatch_workspace_size", "moe_dispatch",
     "moe_permute", "moe_combine", "moe_status_string", "moe_abi_version", "moe_dispatch_noalloc",
     "moe_combine_residual", "moe_dispatch_ex", "moe_permute_ex", "moe_route_stats", "moe_load_stats",
+    "moe_dispatch_ep",
 )
 
 SCALE_FP32, SCALE_UE8M0 = 0, 1
@@ -102,6 +103,8 @@ def lib():
     L.moe_route_stats.restype = I32
     L.moe_load_stats.argtypes = [P, I32, P, I64, ctypes.c_float, P, P]
     L.moe_load_stats.restype = I32
+    L.moe_dispatch_ep.argtypes = [P, P, I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+    L.moe_dispatch_ep.restype = I32
     L.moe_dispatch_ex.argtypes = [P, P, I64, I32, I32, I32, P, P, P, P, P, P, P, I32, P, P, SZ, P]
     L.moe_dispatch_ex.restype = I32
     L.moe_permute_ex.argtypes = [P, P, I64, I32, I32, P, P, P, I32, P, P]
@@ -293,6 +296,56 @@ def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, f
         _ptr(out.X_fp8) if has_x else None, _ptr(out.X_scale) if has_x else None, fmt,
         _ptr(status), _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
     _check(code, "moe_dispatch_ex")
+    return out
+
+
+@dataclass
+class DispatchEP:
+    expert_counts: torch.Tensor
+    expert_offsets: torch.Tensor
+    row_map: torch.Tensor
+    rank_counts: torch.Tensor
+    rank_offsets: torch.Tensor
+    send_token: torch.Tensor
+    slot_send_row: torch.Tensor
+    expand_idx: torch.Tensor
+    send_meta: torch.Tensor
+    X_send: Optional[torch.Tensor] = None
+
+
+def dispatch_ep(topk_idx: torch.Tensor, E: int, ep_size: int, X: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None, status=None, stream=None) -> DispatchEP:
+    """Expert-parallel dispatch metadata with token deduplication (moe_dispatch_ep).
+    send_token / X_send have N*min(K, ep_size) rows; rank_offsets[-1] of them are used."""
+    N, K = topk_idx.shape
+    _need(topk_idx, "topk_idx", torch.int32)
+    dev = topk_idx.device
+    H = 0
+    if X is not None:
+        _need(X, "X", torch.bfloat16)
+        if X.shape[0] != N:
+            raise ValueError("X and topk_idx disagree on N")
+        H = X.shape[1]
+    if ep_size < 1 or E % ep_size != 0:
+        raise ValueError("ep_size must divide E")
+    R, P = ep_size, E // ep_size
+    rows = N * min(K, R)
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = DispatchEP(
+        expert_counts=torch.empty(E, **i32), expert_offsets=torch.empty(E + 1, **i32),
+        row_map=torch.empty(N * K, **i32), rank_counts=torch.empty(R, **i32),
+        rank_offsets=torch.empty(R + 1, **i32), send_token=torch.empty(max(rows, 1), **i32),
+        slot_send_row=torch.empty(N * K, **i32), expand_idx=torch.empty(N * K, **i32),
+        send_meta=torch.empty((R, P + 1), **i32),
+        X_send=torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if X is not None else None)
+    if workspace is None:
+        workspace = dispatch_workspace(E, dev, stream)
+    code = lib().moe_dispatch_ep(
+        _ptr(topk_idx), _ptr(X), N, H, E, K, ep_size, _ptr(out.expert_counts), _ptr(out.expert_offsets),
+        _ptr(out.row_map), _ptr(out.rank_counts), _ptr(out.rank_offsets), _ptr(out.send_token),
+        _ptr(out.slot_send_row), _ptr(out.expand_idx), _ptr(out.send_meta), _ptr(out.X_send), _ptr(status),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(code, "moe_dispatch_ep")
     return out
 
 

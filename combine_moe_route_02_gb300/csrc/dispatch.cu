@@ -86,6 +86,7 @@ struct MetaSmem {
 };
 
 constexpr uint16_t kInvalid = 0xFFFFu;
+constexpr uint16_t kIgnore = 0xFFFEu;   // a slot that takes no row and is not an error
 
 // The CTA's slots are first copied into shared memory as 16-bit expert ids
 // (0xFFFF marks an id outside [0,E)) with every load in flight at once; both
@@ -456,6 +457,7 @@ struct FusedParams {
     int32_t *status;
     unsigned *bar;  // [0] arrive, [1] depart
     int32_t *hist;  // [gridDim.x][E]
+    int ep_P;       // 0: keys are the expert ids; > 0: keys are EP ranks (E of them, ep_P experts each)
 };
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
@@ -530,14 +532,32 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
         quant_row_batch<kFp8, CPL>(xpre, qpre, spre, p.Xs.ue8m0);
     }
 
-    // ---- stage the CTA's expert ids (0xFFFF: out of range)
+    // ---- stage the CTA's keys (0xFFFF: out of range)
     bool bad = false;
+    if (p.ep_P == 0) {
 #pragma unroll 4
-    for (int i = tid; i < ns; i += kFusedThreads) {
-        const int e = p.topk_idx[s0 + i];
-        const bool ok = e >= 0 && e < E;
-        bad |= !ok;
-        stage[i] = ok ? static_cast<uint16_t>(e) : kInvalid;
+        for (int i = tid; i < ns; i += kFusedThreads) {
+            const int e = p.topk_idx[s0 + i];
+            const bool ok = e >= 0 && e < E;
+            bad |= !ok;
+            stage[i] = ok ? static_cast<uint16_t>(e) : kInvalid;
+        }
+    } else {
+        // EP ranks with deduplication: a slot's key is the rank of its expert if no
+        // earlier slot of the same token goes to that rank, else it is ignored (no row)
+        const int P = p.ep_P;
+        for (int i = tid; i < ns; i += kFusedThreads) {
+            const int e = p.topk_idx[s0 + i];
+            const bool ok = e >= 0 && e < E * P;
+            bad |= !ok;
+            const int k = i % K;  // CTA slot ranges start at token boundaries
+            bool first = true;
+            for (int j = i - k; j < i; ++j) {
+                const int ej = p.topk_idx[s0 + j];
+                first &= !(ej >= 0 && ej < E * P && ej / P == e / P);
+            }
+            stage[i] = !ok ? kInvalid : first ? static_cast<uint16_t>(e / P) : kIgnore;
+        }
     }
     if (bad) sm.bad = 1;
     __syncthreads();
@@ -838,11 +858,21 @@ cudaError_t launch_fused_cpl(const FusedParams &p, int grid, size_t smem, cudaSt
     return launch_fused_t<B, F, 1>(p, grid, smem, stream, dev);
 }
 
+bool dispatch_fused_supported(int64_t N, int K, int device)
+{
+    const int sms = device_sm_count(device);
+    int64_t grid = sms;
+    if (grid > N) grid = N;
+    if (grid < 1) return true;
+    const int64_t tok_per = (N + grid - 1) / grid;
+    grid = (N + tok_per - 1) / tok_per;
+    return tok_per * K <= kFusedMaxSlots && grid <= kFusedMaxCtas;
+}
+
 cudaError_t launch_dispatch_fused(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
                                   int32_t *counts, int32_t *offsets, int32_t *row_map, int32_t *src_slot,
                                   void *X_perm, void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status,
-                                  void *workspace,
-                                  size_t workspace_bytes, cudaStream_t stream)
+                                  void *workspace, size_t workspace_bytes, cudaStream_t stream, int ep_P)
 {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -873,6 +903,7 @@ cudaError_t launch_dispatch_fused(const int32_t *topk_idx, const void *X, int64_
     p.status = status;
     p.bar = static_cast<unsigned *>(workspace);
     p.hist = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + 256);
+    p.ep_P = ep_P;
     const size_t slots = static_cast<size_t>(tok_per) * K;
     const size_t smem = sizeof(FusedSmem) + sizeof(int) * kFusedWarps * E + sizeof(int) * slots +
                         ((sizeof(uint16_t) * slots + 15) & ~size_t(15));

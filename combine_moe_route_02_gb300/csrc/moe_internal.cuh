@@ -301,7 +301,9 @@ cudaError_t launch_dispatch_meta(const int32_t *topk_idx, int64_t N, int E, int 
 cudaError_t launch_dispatch_fused(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
                                   int32_t *counts, int32_t *offsets, int32_t *row_map, int32_t *src_slot,
                                   void *X_perm, void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status,
-                                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+                                  void *workspace, size_t workspace_bytes, cudaStream_t stream, int ep_P = 0);
+// Whether launch_dispatch_fused takes N tokens of K slots on this device.
+bool dispatch_fused_supported(int64_t N, int K, int device);
 size_t fused_workspace_bytes(int E);
 
 // X_scale: fp32 [N*K, H/128], or (scale_ue8m0 != 0) one UE8M0 byte per block.

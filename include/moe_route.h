@@ -204,6 +204,45 @@ MOE_API moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X,
                            moe_stream_t stream);
 
 /*
+ * moe_dispatch_ep -- expert-parallel dispatch metadata with token
+ * deduplication for the tokens of one GPU: the metadata of
+ * fused_dedup_prepare_dispatch on the PithTrain page (§8.2 O(n) counting sort
+ * 替代 O(n log n) argsort: counts per expert and per EP rank, prefix sums,
+ * send metadata, dedup scatter, counting sort, expand_idx).  The all-to-all
+ * that moves the rows between GPUs is not part of this library.
+ * The E experts are split over R = ep_size ranks, P = E / R consecutive
+ * experts each (rank(e) = e / P).  A token is sent to a rank once, however
+ * many of its K experts live there.
+ *   expert_counts, expert_offsets, row_map   as moe_dispatch (int32 [E], [E+1], [N*K])
+ *   rank_counts[r]    int32 [R]: tokens sent to rank r (deduplicated)
+ *   rank_offsets[r]   int32 [R+1]: exclusive prefix, rank_offsets[R] = send rows
+ *   send_token[row]   int32 [N*min(K,R)]: the token of send row `row`; rows are
+ *                     ordered by (rank, token)
+ *   slot_send_row[s]  int32 [N*K]: the send row carrying the token of slot s to
+ *                     the rank of its expert
+ *   expand_idx[q]     int32 [N*K]: for row q of the expert-contiguous order
+ *                     (slot s), the index of s's token among its rank's send
+ *                     rows: slot_send_row[s] - rank_offsets[rank(topk_idx[s])]
+ *                     (what the receiving rank gathers its expert rows by)
+ *   send_meta         int32 [R, P+1]: per rank, the dedup token count, then the
+ *                     slot count of each of its P experts
+ *   X_send            bf16 [N*min(K,R), H] or NULL: X_send[row] = X[send_token[row]]
+ *                     (needs X)
+ *   workspace         as moe_dispatch (moe_dispatch_workspace_size(N, E, K) bytes)
+ * Three launches on `stream`.  Errors: as moe_dispatch; MOE_ERR_INVALID_ARG
+ * if ep_size < 1, ep_size > E or E % ep_size != 0; MOE_ERR_UNSUPPORTED beyond
+ * the one-launch dispatch's size limit (the workspace is required).  An expert
+ * index outside [0,E) is reported in status_word; its slot gets no rows.
+ */
+MOE_API moe_status moe_dispatch_ep(const int32_t *topk_idx, const void *X,
+                           int64_t N, int H, int E, int K, int ep_size,
+                           int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map,
+                           int32_t *rank_counts, int32_t *rank_offsets,
+                           int32_t *send_token, int32_t *slot_send_row, int32_t *expand_idx,
+                           int32_t *send_meta, void *X_send, int32_t *status_word,
+                           void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
  * moe_dispatch_noalloc -- moe_dispatch without a caller-provided workspace.
  * The pages have no counterpart: this is a convenience of this library for
  * callers that cannot allocate device memory when they dispatch -- engines that

@@ -127,6 +127,12 @@ def test_permute_and_combine_validation(L):
     assert L.moe_load_stats(A, 257, None, 0, ctypes.c_float(1e-3), A2, None) == INVALID
     assert L.moe_load_stats(None, 16, None, 0, ctypes.c_float(1e-3), A2, None) == INVALID
     assert L.moe_load_stats(A, 16, None, 0, ctypes.c_float(1e-3), A2 + 2, None) == MISALIGNED
+    # expert-parallel metadata: ep_size must divide E; the workspace is required
+    ep = lambda R, ws=0x60000, nb=1 << 20: L.moe_dispatch_ep(A, None, 8, 0, 16, 2, R, A, A2, A3, A4, A, A2, A3, A4,
+                                                             A, None, None, ws, nb, None)
+    assert ep(0) == INVALID and ep(3) == INVALID and ep(32) == INVALID
+    assert ep(4, ws=None, nb=0) == WORKSPACE
+    assert ep(4, ws=0x60000 + 16) == MISALIGNED
     R = 0x50000
     assert L.moe_combine_residual(A, A2, A3, R, 0, 64, 2, A4, None, None) == OK
     assert L.moe_combine_residual(A, A2, A3, None, 8, 64, 2, A4, None, None) == INVALID

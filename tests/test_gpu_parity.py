@@ -230,6 +230,40 @@ def test_dispatch_bad_index_reports_status(fused):
     assert st.item() == moe.ERR_BAD_INDEX
 
 
+@pytest.mark.parametrize("N,E,K,R,H", [(1, 4, 1, 2, 0), (9, 8, 3, 4, 64), (513, 16, 4, 4, 256), (300, 64, 8, 8, 0),
+                                       (2048, 64, 2, 64, 1024), (4096, 64, 4, 1, 0), (16384, 128, 8, 8, 512),
+                                       (20000, 256, 16, 16, 0), (777, 12, 5, 3, 128)])
+def test_dispatch_ep_matches_oracle(N, E, K, R, H):
+    idx = mi.random_topk_idx(N, E, K, seed=N + 3 * E + R)
+    X = mi.random_bf16((N, H), seed=N + H) if H else None
+    st = status_word()
+    d = moe.dispatch_ep(idx.to(DEV), E, R, None if X is None else X.to(DEV), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    o = oracle.dispatch_ep(idx.numpy(), E, R)
+    rows = int(o["rank_offsets"][-1])
+    for k in ("rank_counts", "rank_offsets", "slot_send_row", "expand_idx", "row_map"):
+        assert np.array_equal(getattr(d, k).cpu().numpy().ravel(), o[k].ravel()), k
+    assert np.array_equal(d.expert_counts.cpu().numpy(), o["counts"])
+    assert np.array_equal(d.expert_offsets.cpu().numpy(), o["offsets"])
+    assert np.array_equal(d.send_token[:rows].cpu().numpy(), o["send_token"])
+    assert np.array_equal(d.send_meta.cpu().numpy(), o["send_meta"])
+    if X is not None:
+        assert np.array_equal(bits(d.X_send[:rows]), bits(X)[o["send_token"]])
+
+
+def test_dispatch_ep_bad_index_reports_status():
+    N, E, K, R = 100, 16, 3, 4
+    idx = mi.random_topk_idx(N, E, K, seed=9)
+    idx[7, 2] = E
+    st = status_word()
+    d = moe.dispatch_ep(idx.to(DEV), E, R, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == moe.ERR_BAD_INDEX
+    assert int(d.slot_send_row[7 * K + 2]) == -1
+    assert int(d.expert_counts.sum()) == N * K - 1
+
+
 # ------------------------------------------------------------------ permute
 
 PERMUTE_CASES = [(1, 8, 1, False), (33, 40, 3, False), (513, 1024, 2, False), (100, 128, 8, True),
