@@ -378,7 +378,10 @@ def run_ours(args, rank, world, local):
         if rc:
             raise RuntimeError(f"a library call failed: {moe.status_string(rc)}")
 
-    kernels_per_step = 5 if args.ep_size else 3   # moe_dispatch_ep is three launches
+    # route + dispatch + combine; moe_dispatch_ep is three launches, and moe_dispatch
+    # copies rows in a launch of their own once the copy moves 256 MiB or more
+    copy_bytes = N * (2 * H + 2 * K * H + (K * (H + H // 32) if w.fp8 else 0))
+    kernels_per_step = 5 if args.ep_size else (4 if copy_bytes >= (256 << 20) else 3)
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         step()

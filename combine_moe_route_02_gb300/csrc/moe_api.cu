@@ -10,6 +10,7 @@ namespace moe {
 
 namespace {
 constexpr int kMaxDevices = 64;
+constexpr int64_t kPermuteApartBytes = int64_t(256) << 20;  // row copies this large get their own launch
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_cc_major[kMaxDevices];
 
@@ -23,6 +24,15 @@ moe_status check_topk(int E, int K)
     if (E < 1 || E > 256) return MOE_ERR_INVALID_ARG;
     if (K < 1 || K > 16 || K > E) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
+}
+
+// Bytes the row permute moves: X read once, K bf16 rows and/or K E4M3 rows + scales written.
+int64_t permute_bytes(int64_t N, int H, int K, bool bf16, bool fp8)
+{
+    int64_t per_token = 2 * static_cast<int64_t>(H);
+    if (bf16) per_token += 2 * static_cast<int64_t>(K) * H;
+    if (fp8) per_token += static_cast<int64_t>(K) * (H + H / 32);
+    return N * per_token;
 }
 
 moe_status check_rows(int64_t N, int K)
@@ -217,10 +227,18 @@ moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, in
         return MOE_OK;
     }
     if (use_ws) {
-        const cudaError_t f = launch_dispatch_fused(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map,
-                                                    src_slot, X_perm, X_fp8, X_scale, ue8m0, status_word,
-                                                    workspace, workspace_bytes, s);
-        if (f == cudaSuccess) return MOE_OK;
+        // Large row copies run as a second launch: the permute kernel keeps up to
+        // 64 warps per SM storing (the one-launch kernel has 16), which pays for
+        // the extra launch once the copy moves a few hundred MB.
+        const bool copy_apart = X != nullptr && permute_bytes(N, H, K, X_perm != nullptr, X_fp8 != nullptr) >=
+                                                    kPermuteApartBytes;
+        const cudaError_t f = launch_dispatch_fused(topk_idx, copy_apart ? nullptr : X, N, H, E, K, expert_counts,
+                                                    expert_offsets, row_map, src_slot, X_perm, X_fp8, X_scale, ue8m0,
+                                                    status_word, workspace, workspace_bytes, s);
+        if (f == cudaSuccess) {
+            if (!copy_apart) return MOE_OK;
+            return from_cuda(launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, ue8m0, status_word, s));
+        }
         if (f != cudaErrorNotSupported) return MOE_ERR_CUDA;
     }
     cudaError_t e = launch_dispatch_meta(topk_idx, N, E, K, expert_counts, expert_offsets, row_map, src_slot,

@@ -170,6 +170,11 @@ MOE_API size_t moe_dispatch_workspace_size(int64_t N, int E, int K);
  *   workspace       device scratch of moe_dispatch_workspace_size() bytes
  * An index outside [0,E) is reported in status_word; the outputs are then
  * unspecified but every write stays inside the buffers described above.
+ * Launches: with a workspace, one cooperative launch counts, scans, scatters
+ * and copies the rows; when the row copy moves 256 MiB or more (X read once
+ * plus the rows written) the copy runs as a second launch of the permute
+ * kernel instead.  Without a workspace: one cluster launch for the metadata,
+ * then the permute kernel.
  */
 MOE_API moe_status moe_dispatch(const int32_t *topk_idx, const void *X,
                         int64_t N, int H, int E, int K,

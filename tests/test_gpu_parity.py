@@ -317,6 +317,41 @@ def test_dispatch_with_rows_matches_oracle(N, H, E, K, fp8, bf16, fused):
         assert np.array_equal(d.X_scale.cpu().numpy(), ref[2])
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_dispatch_large_copy_in_its_own_launch(fp8):
+    # a row copy of >= 256 MiB runs as a second launch (the permute kernel) after
+    # the one-launch metadata; a bad id is still reported and skipped
+    N, H, E, K = 40000, 2048, 64, 4
+    X = mi.random_bf16((N, H), seed=51)
+    idx = mi.random_topk_idx(N, E, K, seed=52)
+    idx[123, 3] = E
+    st = status_word()
+    d = moe.dispatch(idx.to(DEV), E, X.to(DEV), fp8=fp8, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == moe.ERR_BAD_INDEX
+    idx_ok = mi.random_topk_idx(N, E, K, seed=52)
+    st.zero_()
+    d = moe.dispatch(idx_ok.to(DEV), E, X.to(DEV), fp8=fp8, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    c, o, r, src = oracle.dispatch(idx_ok.numpy(), E)
+    assert np.array_equal(d.row_map.cpu().numpy(), r) and np.array_equal(d.expert_offsets.cpu().numpy(), o)
+    rows = np.random.default_rng(5).choice(N * K, 3000, replace=False)
+    xb = bits(X)
+    assert np.array_equal(bits(d.X_perm[torch.from_numpy(rows).to(DEV)]), xb[src[rows] // K])
+    if fp8:
+        # the E4M3 rows of the sampled tokens, against the oracle on those tokens alone
+        toks = src[rows] // K
+        uniq = np.unique(toks)
+        one = np.arange(len(uniq) * K, dtype=np.int32)
+        _, rq, rs = oracle.permute(xb[uniq], one, K, fp8=True)
+        pos = {t: i for i, t in enumerate(uniq)}
+        got_q = d.X_fp8[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+        got_s = d.X_scale[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+        for g, t in enumerate(toks):
+            assert np.array_equal(got_q[g], rq[pos[t] * K]) and np.array_equal(got_s[g], rs[pos[t] * K])
+
+
 def test_dispatch_workspace_reused_many_times():
     # the barrier counters must return to zero after every call
     E = 64
