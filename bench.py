@@ -386,10 +386,14 @@ def run_ours(args, rank, world, local):
         if rc:
             raise RuntimeError(f"a library call failed: {moe.status_string(rc)}")
 
-    # route + dispatch + combine; moe_dispatch_ep is three launches, and moe_dispatch
-    # copies rows in a launch of their own once the copy moves 256 MiB or more
+    # route + dispatch + combine; moe_dispatch copies rows in a launch of their own
+    # once the copy moves 256 MiB or more (moe_dispatch_ep likewise for its send rows)
     copy_bytes = N * (2 * H + 2 * K * H + (K * (H + H // 32) if w.fp8 else 0))
-    kernels_per_step = 5 if args.ep_size else (4 if copy_bytes >= (256 << 20) else 3)
+    ep_copy_bytes = N * 2 * H + N * min(K, args.ep_size or 1) * 2 * H
+    if args.ep_size:       # two counting-sort passes, a fix-up, and the send-row copy apart when large
+        kernels_per_step = 2 + 3 + (1 if ep_copy_bytes >= (256 << 20) else 0)
+    else:
+        kernels_per_step = 4 if copy_bytes >= (256 << 20) else 3
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         step()
@@ -562,6 +566,7 @@ def run_ours(args, rank, world, local):
         pg.destroy_process_group()
         return
 
+    load = moe.load_stats(d.expert_counts).cpu().tolist()   # untimed: moe_load_stats on the step's counts
     peak, peak_src = measured_peaks()
     kb = kernel_bytes(w, args.residual, args.scale_format == "ue8m0", ep_rows)
     kern = {}
@@ -594,6 +599,7 @@ def run_ours(args, rank, world, local):
                         "latency_ms: one step alone, nothing overlapped, L2 flushed before"},
         "clocks": sampler.summary(t0, t2) if sampler else None,
         "graph": graph,
+        "load": {"max_over_mean": load[0], "p95_over_mean": load[1], "mean_slots_per_expert": load[3]},
         "timing": ("value: K steps, one event pair per step; kernels: a second pass of min(K,1000) "
                    "steps with an event pair per call"),
     }

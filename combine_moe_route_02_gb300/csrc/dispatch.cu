@@ -401,7 +401,7 @@ __device__ __forceinline__ void copy_token_rows(const uint4 *__restrict__ src, i
 template <bool kBf16Out, bool kFp8, int CPL>
 __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(
     const uint4 *__restrict__ X, const int32_t *__restrict__ row_map, int64_t N, int H, int K,
-    uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq, const ScaleOut Xs, int32_t *status)
+    uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq, const ScaleOut Xs, int32_t *status, int skip_unset)
 {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(
         if (lane < K) {
             my_row = row_map[n * K + lane];
             if (my_row < 0 || my_row >= rows) {
-                bad = true;
+                bad |= !(skip_unset && my_row == -1);  // -1: a slot that takes no row, when allowed
                 my_row = -1;
             }
         }
@@ -762,7 +762,8 @@ cudaError_t launch_dispatch_meta(const int32_t *topk_idx, int64_t N, int E, int 
 }
 
 cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm,
-                           void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status, cudaStream_t stream)
+                           void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status, cudaStream_t stream,
+                           bool skip_unset)
 {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -788,7 +789,8 @@ cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int
     int cpl = chunks > 256 ? 16 : chunks > 128 ? 8 : chunks > 64 ? 4 : chunks > 32 ? 2 : 1;
     if (X_fp8 && cpl > 8) cpl = 8;  // codes and scales stay live too
 #define MOE_PERMUTE_LAUNCH(B, F, C) \
-    return cudaLaunchKernelEx(&cfg, permute_kernel<B, F, C>, x, row_map, N, H, K, xp, xq, xs, status)
+    return cudaLaunchKernelEx(&cfg, permute_kernel<B, F, C>, x, row_map, N, H, K, xp, xq, xs, status, \
+                              skip_unset ? 1 : 0)
 #define MOE_PERMUTE_CPL8(B, F)                         \
     switch (cpl) {                                     \
     case 1: MOE_PERMUTE_LAUNCH(B, F, 1);               \

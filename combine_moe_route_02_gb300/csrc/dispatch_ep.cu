@@ -91,6 +91,7 @@ extern "C" MOE_API moe_status moe_dispatch_ep(const int32_t *topk_idx, const voi
                                               int32_t *send_meta, void *X_send, int32_t *status_word,
                                               void *workspace, size_t workspace_bytes, moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_dispatch_ep");
     if (E < 1 || E > 256 || K < 1 || K > 16 || K > E || N < 0) return MOE_ERR_INVALID_ARG;
     if (N > 0 && N > (static_cast<int64_t>(0x7fffffff) - 1) / K) return MOE_ERR_INVALID_ARG;
     if (ep_size < 1 || ep_size > E || E % ep_size != 0) return MOE_ERR_INVALID_ARG;
@@ -129,10 +130,19 @@ extern "C" MOE_API moe_status moe_dispatch_ep(const int32_t *topk_idx, const voi
                                           expand_idx, nullptr, nullptr, nullptr, 0, status_word, workspace,
                                           workspace_bytes, s, 0);
     if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
-    // 2. EP ranks as keys with deduplication; the first slot of each send row goes to send_token
-    e = launch_dispatch_fused(topk_idx, X, N, X ? H : 0, R, K, rank_counts, rank_offsets, slot_send_row, send_token,
-                              X_send, nullptr, nullptr, 0, status_word, workspace, workspace_bytes, s, P);
+    // 2. EP ranks as keys with deduplication; the first slot of each send row goes to send_token.
+    // A large send-row copy runs as its own permute launch (more warps storing), before the
+    // fix-up fills in the slots that take no row of their own
+    const int64_t max_rows = N * (K < R ? K : R);
+    const bool copy_apart = X != nullptr && N * 2 * static_cast<int64_t>(H) + max_rows * 2 * H >= kPermuteApartBytes;
+    e = launch_dispatch_fused(topk_idx, copy_apart ? nullptr : X, N, X ? H : 0, R, K, rank_counts, rank_offsets,
+                              slot_send_row, send_token, X_send, nullptr, nullptr, 0, status_word, workspace,
+                              workspace_bytes, s, P);
     if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+    if (copy_apart) {
+        e = launch_permute(X, slot_send_row, N, H, K, X_send, nullptr, nullptr, 0, status_word, s, true);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
     // 3. fix-up
     const int sms = device_sm_count(dev);
     const int64_t need = (N * K + kFixThreads - 1) / kFixThreads;

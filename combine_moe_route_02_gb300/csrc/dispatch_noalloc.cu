@@ -58,6 +58,7 @@ extern "C" MOE_API moe_status moe_dispatch_noalloc(const int32_t *topk_idx, cons
                                                    int32_t *row_map, int32_t *src_slot, void *X_perm, void *X_fp8,
                                                    float *X_scale, int32_t *status_word, moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_dispatch_noalloc");
     // The same argument checks as moe_dispatch, which then runs with this
     // library's own scratch as its workspace.
     if (E < 1 || E > 256 || K < 1 || K > 16 || K > E || N < 0) return MOE_ERR_INVALID_ARG;

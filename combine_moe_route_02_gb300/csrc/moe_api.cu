@@ -10,7 +10,6 @@ namespace moe {
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int64_t kPermuteApartBytes = int64_t(256) << 20;  // row copies this large get their own launch
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_cc_major[kMaxDevices];
 
@@ -93,6 +92,7 @@ moe_status moe_route_ex(const void *X, const void *W_gate, const float *bias, in
                         int renorm, int32_t *topk_idx, float *topk_w, int32_t *status_word, int algo,
                         moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_route");
     moe_status st = check_topk(E, K);
     if (st != MOE_OK) return st;
     if ((st = check_rows(N, K)) != MOE_OK) return st;
@@ -119,6 +119,7 @@ moe_status moe_route_stats(const void *X, const void *W_gate, const float *bias,
                            int renorm, int32_t *topk_idx, float *topk_w, float *lse, int32_t *expert_counts,
                            int32_t *status_word, int algo, moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_route_stats");
     moe_status st = check_topk(E, K);
     if (st != MOE_OK) return st;
     if ((st = check_rows(N, K)) != MOE_OK) return st;
@@ -154,6 +155,7 @@ moe_status moe_route_stats(const void *X, const void *W_gate, const float *bias,
 moe_status moe_load_stats(const int32_t *expert_counts, int E, const float *lse, int64_t N, float z_coef,
                           float *stats, moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_load_stats");
     if (E < 1 || E > 256 || N < 0) return MOE_ERR_INVALID_ARG;
     if (!expert_counts || !stats) return MOE_ERR_INVALID_ARG;
     if (!aligned4(expert_counts) || !aligned4(stats) || (lse && !aligned4(lse))) return MOE_ERR_MISALIGNED;
@@ -199,6 +201,7 @@ moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, in
                            void *X_perm, void *X_fp8, void *X_scale, int scale_format, int32_t *status_word,
                            void *workspace, size_t workspace_bytes, moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_dispatch");
     moe_status st = check_topk(E, K);
     if (st != MOE_OK) return st;
     if ((st = check_rows(N, K)) != MOE_OK) return st;
@@ -263,6 +266,7 @@ moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H
 moe_status moe_permute_ex(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm,
                           void *X_fp8, void *X_scale, int scale_format, int32_t *status_word, moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_permute");
     if (K < 1 || K > 16) return MOE_ERR_INVALID_ARG;
     if (scale_format != MOE_SCALE_FP32 && scale_format != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     moe_status st = check_rows(N, K);
@@ -299,6 +303,7 @@ static moe_status validate_combine(const void *Y, const int32_t *row_map, const 
 moe_status moe_combine(const void *Y, const int32_t *row_map, const float *topk_w, int64_t N, int H, int K,
                        void *out, int32_t *status_word, moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_combine");
     const moe_status st = validate_combine(Y, row_map, topk_w, N, H, K, out, status_word);
     if (st != MOE_OK || N == 0) return st;
     return from_cuda(launch_combine(Y, row_map, topk_w, nullptr, N, H, K, out, status_word,
@@ -308,6 +313,7 @@ moe_status moe_combine(const void *Y, const int32_t *row_map, const float *topk_
 moe_status moe_combine_residual(const void *Y, const int32_t *row_map, const float *topk_w, const void *residual,
                                 int64_t N, int H, int K, void *out, int32_t *status_word, moe_stream_t stream)
 {
+    NvtxRange nvtx_range("moe_combine_residual");
     const moe_status st = validate_combine(Y, row_map, topk_w, N, H, K, out, status_word);
     if (st != MOE_OK || N == 0) return st;
     if (!residual) return MOE_ERR_INVALID_ARG;

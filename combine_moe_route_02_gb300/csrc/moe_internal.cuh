@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/moe_route.h"
 
 namespace moe {
@@ -307,12 +309,25 @@ bool dispatch_fused_supported(int64_t N, int K, int device);
 size_t fused_workspace_bytes(int E);
 
 // X_scale: fp32 [N*K, H/128], or (scale_ue8m0 != 0) one UE8M0 byte per block.
+// skip_unset: a row_map entry of -1 means "no row" and is not reported.
 cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int H, int K, void *X_perm,
-                           void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status, cudaStream_t stream);
+                           void *X_fp8, void *X_scale, int scale_ue8m0, int32_t *status, cudaStream_t stream,
+                           bool skip_unset = false);
+// Row copies at least this large run as their own launch of the permute kernel.
+constexpr int64_t kPermuteApartBytes = int64_t(256) << 20;
 
 // residual: NULL for the plain weighted combine.
 cudaError_t launch_combine(const void *Y, const int32_t *row_map, const float *w, const void *residual, int64_t N,
                            int H, int K, void *out, int32_t *status, cudaStream_t stream);
+
+// Names one C-ABI call on a profiler's timeline (NVTX push/pop; without a
+// profiler attached the calls return at once).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count(int device);

@@ -233,7 +233,7 @@ def test_dispatch_bad_index_reports_status(fused):
 
 @pytest.mark.parametrize("N,E,K,R,H", [(1, 4, 1, 2, 0), (9, 8, 3, 4, 64), (513, 16, 4, 4, 256), (300, 64, 8, 8, 0),
                                        (2048, 64, 2, 64, 1024), (4096, 64, 4, 1, 0), (16384, 128, 8, 8, 512),
-                                       (20000, 256, 16, 16, 0), (777, 12, 5, 3, 128)])
+                                       (20000, 256, 16, 16, 0), (777, 12, 5, 3, 128), (20000, 64, 8, 8, 2048)])
 def test_dispatch_ep_matches_oracle(N, E, K, R, H):
     idx = mi.random_topk_idx(N, E, K, seed=N + 3 * E + R)
     X = mi.random_bf16((N, H), seed=N + H) if H else None
@@ -250,7 +250,10 @@ def test_dispatch_ep_matches_oracle(N, E, K, R, H):
     assert np.array_equal(d.send_token[:rows].cpu().numpy(), o["send_token"])
     assert np.array_equal(d.send_meta.cpu().numpy(), o["send_meta"])
     if X is not None:
-        assert np.array_equal(bits(d.X_send[:rows]), bits(X)[o["send_token"]])
+        # all send rows, or (for large copies, which run as a separate permute launch) a sample
+        pick = np.arange(rows) if rows * H <= (1 << 26) else np.random.default_rng(7).choice(rows, 4000, False)
+        got = bits(d.X_send[torch.from_numpy(pick).to(DEV)])
+        assert np.array_equal(got, bits(X)[o["send_token"][pick]])
 
 
 def test_dispatch_ep_bad_index_reports_status():
