@@ -40,7 +40,7 @@ import moe_inputs as mi  # noqa: E402
 METRIC = "route+dispatch+combine tokens/s on 1 GB300; % of HBM roofline per kernel"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-E2E_UNIT = 16          # pipelined end-to-end steps per CUDA graph
+E2E_UNIT = 64          # pipelined end-to-end steps per CUDA graph
 L2_FLUSH_BYTES = 256 << 20
 
 
