@@ -20,9 +20,9 @@ import torch
 from . import _build
 
 __all__ = [
-    "build", "lib", "MoeError", "route", "dispatch", "permute", "combine",
-    "dispatch_workspace_size", "dispatch_workspace", "status_string", "ROUTE_AUTO", "ROUTE_TCGEN05", "ROUTE_SIMT",
-    "Dispatch",
+    "build", "lib", "MoeError", "route", "route_stats", "load_stats", "dispatch", "dispatch_ep", "permute",
+    "combine", "dispatch_workspace_size", "dispatch_workspace", "status_string", "ROUTE_AUTO", "ROUTE_TCGEN05",
+    "ROUTE_SIMT", "SCALE_FP32", "SCALE_UE8M0", "Dispatch", "DispatchEP",
 ]
 
 MOE_OK = 0
@@ -259,10 +259,11 @@ def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, f
              stream=None, scale_format: str = "fp32") -> Dispatch:
     """Counting-sort dispatch (+ optional row permute / E4M3 quantise).
 
-    fused=True (default) runs the one-launch cooperative kernel with a
-    workspace (a cached zeroed one unless given); fused=False passes no
-    workspace, which selects the single-cluster metadata kernel followed by
-    the permute kernel.  scale_format "fp32" (float scales) or "ue8m0" (one
+    fused=True (default) passes a workspace (a cached zeroed one unless
+    given), which selects the one-launch cooperative kernel (for row copies of
+    256 MiB or more: that kernel for the metadata, then the permute kernel);
+    fused=False passes no workspace, which selects the single-cluster metadata
+    kernel followed by the permute kernel.  scale_format "fp32" (float scales) or "ue8m0" (one
     exponent byte per 1x128 block) selects the E4M3 block-scale output."""
     fmt = _scale_format(scale_format)
     N, K = topk_idx.shape
