@@ -55,6 +55,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-torch-naive", action="store_true", help="skip the stock-PyTorch comparison figure")
     p.add_argument("--scale-format", default="fp32", choices=["fp32", "ue8m0"],
                    help="E4M3 block-scale output of fp8 workloads: fp32 scales or UE8M0 exponent bytes")
     p.add_argument("--ep-size", type=int, default=0,
@@ -258,6 +259,56 @@ def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000, residual:
     return {"value": reps * w.N / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"the whole {w.name} workload ({w.N} tokens), {reps} passes of route+dispatch+permute+"
                       f"combine in fp64 C, {el:.1f} s"}
+
+
+def torch_naive(Xd, Wd, bd, w: mi.Workload, Y, flush, reps: int = 100):
+    """The same step as a chain of stock PyTorch ops on the same GPU (a context figure, not
+    a product path): fp32 logits through HBM, softmax, topk, renorm, stable argsort of the
+    expert ids, index_select for the permute (+ a per-block E4M3 cast for fp8 workloads),
+    and an index_select + weighted sum for the combine."""
+    import torch
+
+    N, H, E, K = w.N, w.H, w.E, w.K
+    ar = torch.arange(N * K, device=Xd.device)
+
+    def step():
+        L = Xd.float() @ Wd.float()
+        if bd is not None:
+            L = L + bd
+        p = torch.softmax(L, dim=1)
+        idx = torch.topk(L, K, dim=1).indices
+        tw = p.gather(1, idx)
+        if w.renorm:
+            tw = tw / tw.sum(dim=1, keepdim=True)
+        flat = idx.flatten()
+        order = torch.argsort(flat, stable=True)              # row -> slot
+        torch.bincount(flat, minlength=E)
+        Xp = Xd.index_select(0, order // K)
+        if w.fp8:
+            blk = Xp.float().view(N * K, H // 128, 128)
+            t = blk.abs().amax(dim=-1, keepdim=True).clamp_min(1e-4) / 448.0
+            s = torch.exp2(torch.ceil(torch.log2(t)))
+            (blk / s).to(torch.float8_e4m3fn)
+        row_map = torch.empty_like(order)
+        row_map[order] = ar
+        (Y.index_select(0, row_map).view(N, K, H).float() * tw.unsqueeze(-1)).sum(dim=1).to(torch.bfloat16)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    m = statistics.fmean(ms)
+    return {"value": N / (m * 1e-3), "unit": UNIT, "ms_per_step": m, "steps": reps,
+            "what": "stock PyTorch ops on the same GPU: fp32 matmul, softmax, topk, renorm, stable argsort, "
+                    "index_select permute (+ E4M3 cast), index_select + weighted sum; L2 flushed between steps"}
 
 
 def run_reference(args, rank, world):
@@ -567,6 +618,7 @@ def run_ours(args, rank, world, local):
         return
 
     load = moe.load_stats(d.expert_counts).cpu().tolist()   # untimed: moe_load_stats on the step's counts
+    naive = torch_naive(Xd, Wd, bd, w, Y, flush, reps=min(args.steps, 100)) if not args.no_torch_naive else None
     peak, peak_src = measured_peaks()
     kb = kernel_bytes(w, args.residual, args.scale_format == "ue8m0", ep_rows)
     kern = {}
@@ -600,6 +652,7 @@ def run_ours(args, rank, world, local):
         "clocks": sampler.summary(t0, t2) if sampler else None,
         "graph": graph,
         "load": {"max_over_mean": load[0], "p95_over_mean": load[1], "mean_slots_per_expert": load[3]},
+        "torch_naive": naive,
         "timing": ("value: K steps, one event pair per step; kernels: a second pass of min(K,1000) "
                    "steps with an event pair per call"),
     }
