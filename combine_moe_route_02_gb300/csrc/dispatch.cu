@@ -443,6 +443,7 @@ constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr int kFusedMaxSlots = 16384;   // slots per CTA staged in shared memory
 constexpr int kFusedMaxCtas = 1024;     // bound used to size the workspace
 constexpr int kHistBatch = 32;          // per-thread count loads in flight at once
+constexpr int kHistBatch4 = 8;          // the same for 16-byte loads of four counts
 
 struct FusedParams {
     const int32_t *topk_idx;
@@ -608,7 +609,37 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
     // Thread (grp, e) sums rows grp, grp + groups, ... of column e; all of its
     // loads are issued before the first add (one L2 round trip), then the
     // per-group partials meet in shared memory.
-    {
+    if (E % 4 == 0) {
+        // four experts per 16-byte load: a quarter of the requests
+        const int E4 = E >> 2;
+        const int groups = kFusedThreads / E4;  // >= 8 (E <= 256)
+        const int e4 = tid % E4;
+        const int grp = tid / E4;
+        int4 tot = make_int4(0, 0, 0, 0), bef = make_int4(0, 0, 0, 0);
+        if (grp < groups) {
+            const int4 *h4 = reinterpret_cast<const int4 *>(p.hist) + e4;
+            for (int c0 = grp; c0 < static_cast<int>(G); c0 += kHistBatch4 * groups) {
+                int4 v[kHistBatch4];
+#pragma unroll
+                for (int i = 0; i < kHistBatch4; ++i) {
+                    const int cc = c0 + i * groups;
+                    v[i] = cc < static_cast<int>(G) ? __ldcg(h4 + static_cast<int64_t>(cc) * E4) : make_int4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int i = 0; i < kHistBatch4; ++i) {
+                    const bool lower = c0 + i * groups < c;
+                    tot.x += v[i].x; tot.y += v[i].y; tot.z += v[i].z; tot.w += v[i].w;
+                    bef.x += lower ? v[i].x : 0; bef.y += lower ? v[i].y : 0;
+                    bef.z += lower ? v[i].z : 0; bef.w += lower ? v[i].w : 0;
+                }
+            }
+            const int e = 4 * e4;
+            atomicAdd(&sm.total[e], tot.x); atomicAdd(&sm.total[e + 1], tot.y);
+            atomicAdd(&sm.total[e + 2], tot.z); atomicAdd(&sm.total[e + 3], tot.w);
+            atomicAdd(&sm.before[e], bef.x); atomicAdd(&sm.before[e + 1], bef.y);
+            atomicAdd(&sm.before[e + 2], bef.z); atomicAdd(&sm.before[e + 3], bef.w);
+        }
+    } else {
         const int groups = kFusedThreads / E;   // >= 2 (E <= 256)
         const int e = tid % E;
         const int grp = tid / E;
