@@ -56,6 +56,9 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-torch-naive", action="store_true", help="skip the stock-PyTorch comparison figure")
+    p.add_argument("--route-stats", action="store_true",
+                   help="route with the router statistics (moe_route_stats: logsumexp + expert histogram) and "
+                        "add moe_load_stats (max/mean, p95/mean, z-loss) to every step")
     p.add_argument("--scale-format", default="fp32", choices=["fp32", "ue8m0"],
                    help="E4M3 block-scale output of fp8 workloads: fp32 scales or UE8M0 exponent bytes")
     p.add_argument("--ep-size", type=int, default=0,
@@ -212,11 +215,16 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- CPU oracle baseline
 
-def oracle_pass(oracle, Xb, Wb, bias, w: mi.Workload, Y, R=None, ue8m0=False, ep_size=0):
+def oracle_pass(oracle, Xb, Wb, bias, w: mi.Workload, Y, R=None, ue8m0=False, ep_size=0, stats=False):
     """One pass of the oracle over the workload: route, dispatch, permute, combine
     (with the residual R when given; UE8M0 block scales when ue8m0; the EP
-    metadata and dedup'd send rows when ep_size)."""
-    idx, tw = oracle.route(Xb, Wb, bias, w.K, w.renorm)
+    metadata and dedup'd send rows when ep_size; the router statistics when stats)."""
+    if stats:
+        idx, tw, L = oracle.route(Xb, Wb, bias, w.K, w.renorm, want_logits=True)
+        counts = np.bincount(idx.ravel(), minlength=w.E).astype(np.int32)
+        oracle.load_stats(counts, oracle.logsumexp(L), 1e-3)
+    else:
+        idx, tw = oracle.route(Xb, Wb, bias, w.K, w.renorm)
     if ep_size:
         ep = oracle.dispatch_ep(idx, w.E, ep_size)
         row_map = ep["row_map"]
@@ -241,7 +249,7 @@ def residual_rows(w: mi.Workload, rank: int = 0):
 
 
 def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000, residual: bool = False,
-                 ue8m0: bool = False, ep_size: int = 0):
+                 ue8m0: bool = False, ep_size: int = 0, stats: bool = False):
     import oracle
     X, W, bias = mi.make_workload_inputs(w)
     Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
@@ -251,7 +259,7 @@ def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000, residual:
     R = mi.bf16_bits(residual_rows(w)) if residual else None
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, ep_size)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, ep_size, stats)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= max_reps:
@@ -323,10 +331,10 @@ def run_reference(args, rank, world):
     R = mi.bf16_bits(residual_rows(w)) if args.residual else None
     ue8m0 = args.scale_format == "ue8m0"
     for _ in range(args.warmup):
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, args.ep_size)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, args.ep_size, args.route_stats)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, args.ep_size)
+        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, args.ep_size, args.route_stats)
     el = time.perf_counter() - t0
     value = args.steps * w.N / el
     sample = f"the whole {w.name} workload ({w.N} tokens) per step, fp64 C oracle"
@@ -344,6 +352,8 @@ def combine_config(args):
     c = {"dispatch": f"moe_dispatch_ep, ep_size {args.ep_size}"} if args.ep_size else {}
     c["combine"] = ("forward_aggregate: weighted sum + residual, one bf16 rounding" if args.residual
                     else "weighted sum")
+    if args.route_stats:
+        c["route"] = "moe_route_stats (logsumexp + expert histogram) and moe_load_stats every step"
     if mi.WORKLOADS[args.workload].fp8:
         c["fp8_scales"] = args.scale_format
     return c
@@ -400,11 +410,19 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         ep_rows = int(de.rank_offsets[-1])
     disp_fn = L.moe_dispatch_ep if args.ep_size else L.moe_dispatch_ex
+    route_fn = L.moe_route_stats if args.route_stats else L.moe_route_ex
+    lse_buf = torch.empty(N, dtype=torch.float32, device=dev) if args.route_stats else None
+    cnt_buf = torch.empty(E, dtype=torch.int32, device=dev) if args.route_stats else None
+    stats_buf = torch.empty(4, dtype=torch.float32, device=dev) if args.route_stats else None
     comb_fn = L.moe_combine if R is None else L.moe_combine_residual
 
     def call_args(xd, o, spp, wsp):
         """Arguments of the three C-ABI calls of one step: tokens from xd, output to o, on stream spp."""
-        ra = (vp(xd), vp(Wd), vp(bd), N, H, E, K, int(w.renorm), vp(idx), vp(tw), vp(st), moe.ROUTE_AUTO, spp)
+        if args.route_stats:
+            ra = (vp(xd), vp(Wd), vp(bd), N, H, E, K, int(w.renorm), vp(idx), vp(tw), vp(lse_buf), vp(cnt_buf),
+                  vp(st), moe.ROUTE_AUTO, spp)
+        else:
+            ra = (vp(xd), vp(Wd), vp(bd), N, H, E, K, int(w.renorm), vp(idx), vp(tw), vp(st), moe.ROUTE_AUTO, spp)
         if de is not None:
             da = (vp(idx), vp(xd), N, H, E, K, args.ep_size, vp(de.expert_counts), vp(de.expert_offsets),
                   vp(de.row_map), vp(de.rank_counts), vp(de.rank_offsets), vp(de.send_token),
@@ -425,13 +443,15 @@ def run_ours(args, rank, world, local):
         rc = 0
         if ev is not None:
             ev[0].record(stream)
-        rc |= L.moe_route_ex(*route_args)
+        rc |= route_fn(*route_args)
         if ev is not None:
             ev[1].record(stream)
         rc |= disp_fn(*disp_args)                  # counting sort + row permute (+ E4M3), one launch
         if ev is not None:
             ev[2].record(stream)
         rc |= comb_fn(*comb_args)
+        if stats_buf is not None:          # load statistics of the step (one small kernel)
+            rc |= L.moe_load_stats(vp(cnt_buf), E, vp(lse_buf), N, ctypes.c_float(1e-3), vp(stats_buf), sp)
         if ev is not None:
             ev[3].record(stream)
         if rc:
@@ -445,6 +465,8 @@ def run_ours(args, rank, world, local):
         kernels_per_step = 2 + 3 + (1 if ep_copy_bytes >= (256 << 20) else 0)
     else:
         kernels_per_step = 4 if copy_bytes >= (256 << 20) else 3
+    if args.route_stats:   # moe_load_stats; moe_route_stats also clears the counts (a memset)
+        kernels_per_step += 1
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         step()
@@ -503,11 +525,11 @@ def run_ours(args, rank, world, local):
         gs.wait_stream(stream)
         with torch.cuda.stream(gs):
             for _ in range(2):  # warm the graph stream's workspace and plans
-                L.moe_route_ex(*g_route); disp_fn(*g_disp); comb_fn(*g_comb)
+                route_fn(*g_route); disp_fn(*g_disp); comb_fn(*g_comb)
         torch.cuda.synchronize()
         cg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg, stream=gs):
-            rc = L.moe_route_ex(*g_route) | disp_fn(*g_disp) | comb_fn(*g_comb)
+            rc = route_fn(*g_route) | disp_fn(*g_disp) | comb_fn(*g_comb)
         if rc:
             raise RuntimeError(moe.status_string(rc))
         gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ksteps)]
@@ -552,7 +574,11 @@ def run_ours(args, rank, world, local):
             if i >= 2:
                 cs.wait_event(ev_d[b])              # Ob[b] of step i-2 has been read back
             ra, da, ca = cargs[b]
-            if L.moe_route_ex(*ra) | disp_fn(*da) | comb_fn(*ca):
+            rc = route_fn(*ra) | disp_fn(*da) | comb_fn(*ca)
+            if stats_buf is not None:
+                rc |= L.moe_load_stats(vp(cnt_buf), E, vp(lse_buf), N, ctypes.c_float(1e-3), vp(stats_buf),
+                                       ctypes.c_void_p(cs.cuda_stream))
+            if rc:
                 raise RuntimeError("a library call failed")
             ev_c[b].record(cs)
             ds.wait_event(ev_c[b])
@@ -658,7 +684,8 @@ def run_ours(args, rank, world, local):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, residual=args.residual,
-                                            ue8m0=args.scale_format == "ue8m0", ep_size=args.ep_size)
+                                            ue8m0=args.scale_format == "ue8m0", ep_size=args.ep_size,
+                                            stats=args.route_stats)
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()

@@ -4,86 +4,124 @@
 // of the counts over the mean, and a z-loss of weight z_coef over the per-token
 // logsumexp of the logits (the page regularises with weight 1e-3).
 //
-// One CTA: the E <= 256 counts are sorted in shared memory (bitonic network)
-// for the percentile, and the squares of the N logsumexp values are summed in
-// fp64 in a fixed order (per-thread strided sums, then a fixed tree), so the
-// result does not depend on scheduling.  This runs once per step next to the
-// router, off the bandwidth-bound path.
+// One CTA of 1024 threads: the squares of the N logsumexp values are summed in a
+// fixed order (each thread a fixed set of elements, 16-byte loads several in
+// flight, Kahan-compensated fp32; the per-thread sums added in fp64 in a fixed
+// order), so the result does not depend on scheduling; the two order statistics the 95th percentile needs are
+// found by ranking each of the E <= 256 counts against the others (ties by
+// index) rather than by sorting.
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kStatThreads = 256;  // also the sort width (E <= 256)
+constexpr int kStatThreads = 1024;
+constexpr int kStatBatch = 8;      // 16-byte loads in flight per thread
 
 __global__ void __launch_bounds__(kStatThreads) load_stats_kernel(const int32_t *__restrict__ counts, int E,
                                                                   const float *__restrict__ lse, int64_t N,
                                                                   float z_coef, float *__restrict__ stats)
 {
-    __shared__ int key[kStatThreads];
-    __shared__ double part[kStatThreads / 32];
-    __shared__ long long tot[kStatThreads / 32];
-    __shared__ int mx[kStatThreads / 32];
+    __shared__ int key[256];
+    __shared__ double zpart[kStatThreads];
+    __shared__ long long tpart[8];
+    __shared__ int mpart[8];
+    __shared__ int q_lo, q_hi;
+    __shared__ double zsum_s;
     const int t = threadIdx.x;
     const int warp = t >> 5;
     const int lane = t & 31;
 
     pdl_wait_prior_grids();
 
-    const int c = t < E ? counts[t] : 0;
-    key[t] = t < E ? c : 0x7fffffff;  // padding sorts to the end
-    long long s = c;
-    int m = c;
-    double z = 0.0;
-    if (lse != nullptr)
-        for (int64_t i = t; i < N; i += kStatThreads) {
-            const double v = lse[i];
-            z += v * v;
-        }
+    if (t < 256) key[t] = t < E ? counts[t] : 0;
+    // sum of lse^2: each thread a fixed set of elements in a fixed order (16-byte
+    // loads, kStatBatch in flight), Kahan-compensated in fp32 -- this GPU's fp64
+    // rate is a small fraction of fp32 -- then the 1024 per-thread sums are added
+    // in fp64 by one warp in a fixed order
+    float zs = 0.f, zc = 0.f;
+    auto kahan = [&](float v) {
+        const float y = v * v - zc;
+        const float u = zs + y;
+        zc = (u - zs) - y;
+        zs = u;
+    };
+    if (lse != nullptr) {
+        int64_t done = 0;
+        if ((reinterpret_cast<uintptr_t>(lse) & 15u) == 0) {
+            const float4 *l4 = reinterpret_cast<const float4 *>(lse);
+            const int64_t n4 = N >> 2;
+            for (int64_t base = t; base < n4; base += static_cast<int64_t>(kStatThreads) * kStatBatch) {
+                float4 v[kStatBatch];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, o);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        z += __shfl_xor_sync(0xffffffffu, z, o);
-    }
-    if (lane == 0) {
-        tot[warp] = s;
-        mx[warp] = m;
-        part[warp] = z;
-    }
-    // ascending bitonic sort of the padded counts
-    for (int size = 2; size <= kStatThreads; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            __syncthreads();
-            const int l = t ^ stride;
-            if (l > t) {
-                const int a = key[t], b = key[l];
-                const bool up = (t & size) == 0;
-                if ((a > b) == up) {
-                    key[t] = b;
-                    key[l] = a;
+                for (int u = 0; u < kStatBatch; ++u) {
+                    const int64_t i = base + static_cast<int64_t>(u) * kStatThreads;
+                    v[u] = i < n4 ? __ldcs(l4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kStatBatch; ++u) {
+                    kahan(v[u].x);
+                    kahan(v[u].y);
+                    kahan(v[u].z);
+                    kahan(v[u].w);
                 }
             }
+            done = n4 << 2;
         }
+        for (int64_t i = done + t; i < N; i += kStatThreads) kahan(lse[i]);
+    }
+    zpart[t] = static_cast<double>(zs) - static_cast<double>(zc);
+    __syncthreads();  // key[] and zpart[] ready
+
+    // total, maximum, and the order statistics around position 0.95 (E - 1): the
+    // count whose rank (ties broken by index) equals lo or hi
+    const double pos = 0.95 * (E - 1);
+    const int lo = static_cast<int>(floor(pos));
+    const int hi = lo + 1 < E ? lo + 1 : E - 1;
+    if (t < 256) {
+        const int c = t < E ? key[t] : 0;
+        long long sum = c;
+        int mx = c;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        if (lane == 0) {
+            tpart[warp] = sum;
+            mpart[warp] = mx;
+        }
+        if (t < E) {
+            int rank = 0;
+            for (int j = 0; j < E; ++j) {
+                const int kj = key[j];
+                rank += (kj < c || (kj == c && j < t)) ? 1 : 0;
+            }
+            if (rank == lo) q_lo = c;
+            if (rank == hi) q_hi = c;
+        }
+    }
+    if (warp == 8) {
+        double acc = 0.0;
+        for (int i = lane; i < kStatThreads; i += 32) acc += zpart[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) zsum_s = acc;
     }
     __syncthreads();
     if (t == 0) {
+        const double zsum = zsum_s;
         long long total = 0;
         int mxc = 0;
-        double zs = 0.0;
-        for (int w = 0; w < kStatThreads / 32; ++w) {
-            total += tot[w];
-            mxc = max(mxc, mx[w]);
-            zs += part[w];
+        for (int w = 0; w < 8; ++w) {
+            total += tpart[w];
+            mxc = max(mxc, mpart[w]);
         }
         const double mean = static_cast<double>(total) / E;
-        const double pos = 0.95 * (E - 1);
-        const int lo = static_cast<int>(floor(pos));
-        const int hi = lo + 1 < E ? lo + 1 : E - 1;
-        const double p95 = key[lo] + (pos - lo) * static_cast<double>(key[hi] - key[lo]);
+        const double p95 = q_lo + (pos - lo) * static_cast<double>(q_hi - q_lo);
         stats[0] = mean > 0.0 ? static_cast<float>(mxc / mean) : 0.f;
         stats[1] = mean > 0.0 ? static_cast<float>(p95 / mean) : 0.f;
-        stats[2] = (lse != nullptr && N > 0) ? static_cast<float>(static_cast<double>(z_coef) * zs / N) : 0.f;
+        stats[2] = (lse != nullptr && N > 0) ? static_cast<float>(static_cast<double>(z_coef) * zsum / N) : 0.f;
         stats[3] = static_cast<float>(mean);
     }
     pdl_launch_dependents();

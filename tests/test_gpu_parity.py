@@ -213,6 +213,23 @@ def test_dispatch_hot_experts(fused):
     assert np.array_equal(d.expert_offsets.cpu().numpy(), o)
 
 
+def test_dispatch_beyond_one_launch_limit_falls_back():
+    # more than 16384 slots per CTA: the one-launch kernel declines and the cluster
+    # metadata kernel takes the call (ids staged partly in shared memory, the rest
+    # read from global memory)
+    N, E, K = 700000, 64, 4
+    idx = mi.random_topk_idx(N, E, K, seed=77)
+    st = status_word()
+    d = moe.dispatch(idx.to(DEV), E, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    c, o, r, src = oracle.dispatch(idx.numpy(), E)
+    assert np.array_equal(d.expert_counts.cpu().numpy(), c)
+    assert np.array_equal(d.expert_offsets.cpu().numpy(), o)
+    assert np.array_equal(d.row_map.cpu().numpy(), r)
+    assert np.array_equal(d.src_slot.cpu().numpy(), src)
+
+
 def test_dispatch_empty_writes_zero_counts():
     idx = torch.empty(0, 2, dtype=torch.int32, device=DEV)
     d = moe.dispatch(idx, 8)
