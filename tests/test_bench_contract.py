@@ -1,0 +1,43 @@
+"""The benchmark's JSON line, checked on the CPU through the reference arm
+(`bench.py --impl reference`, which times the oracle and needs no GPU): one
+line with the keys and types the benchmark contract asks for."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_reference(*extra):
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "1",
+           "--workload", "tiny_n512_h256_e16_k2", *extra]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0])
+
+
+def test_reference_line_has_the_contract_keys():
+    d = run_reference()
+    assert d["impl"] == "reference"
+    for k, t in [("metric", str), ("value", float), ("unit", str), ("n_gpus", int), ("steps", int),
+                 ("warmup", int), ("ms_per_step", float), ("higher_is_better", bool), ("scaling", str),
+                 ("dtype", str), ("data", str), ("config", dict), ("cpu_baseline", dict), ("e2e", dict)]:
+        assert isinstance(d[k], t), k
+    assert d["vs_baseline"] is None
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["config"]["workload"] == "tiny_n512_h256_e16_k2"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+    assert d["value"] > 0 and d["higher_is_better"] is True
+
+
+def test_reference_line_names_the_variant():
+    d = run_reference("--residual", "--route-stats")
+    assert "residual" in d["config"]["combine"]
+    assert "moe_route_stats" in d["config"]["route"]
