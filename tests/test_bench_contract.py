@@ -1,10 +1,13 @@
-"""The benchmark's JSON line, checked on the CPU through the reference arm
-(`bench.py --impl reference`, which times the oracle and needs no GPU): one
-line with the keys and types the benchmark contract asks for."""
+"""The benchmark's JSON line: one line with the keys and types the benchmark
+contract asks for -- on the CPU through the reference arm (`bench.py --impl
+reference`, which times the oracle and needs no GPU), and on a GPU through a
+short run of the CUDA path."""
 import json
 import os
 import subprocess
 import sys
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -41,3 +44,27 @@ def test_reference_line_names_the_variant():
     d = run_reference("--residual", "--route-stats")
     assert "residual" in d["config"]["combine"]
     assert "moe_route_stats" in d["config"]["route"]
+
+
+@pytest.mark.gpu
+def test_gpu_line_has_the_contract_keys():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "5", "--warmup", "3", "--no-cpu-baseline",
+           "--e2e-steps", "16", "--no-torch-naive"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3 and d["value"] > 0
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert "traffic" in r
+    c = d["clocks"]
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(c)
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] >= 3 * d["steps"]
