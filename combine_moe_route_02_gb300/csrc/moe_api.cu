@@ -16,7 +16,14 @@ std::atomic<int> g_cc_major[kMaxDevices];
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-inline moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+// A failed launch is reported by the status alone: the runtime's last-error slot
+// is cleared so that a caller's later, unrelated check does not see it again.
+inline moe_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return MOE_OK;
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+}
 
 moe_status check_topk(int E, int K)
 {
@@ -107,7 +114,7 @@ moe_status moe_route_ex(const void *X, const void *W_gate, const float *bias, in
 
     RouteArgs a{X, W_gate, bias, N, H, E, K, renorm ? 1 : 0, topk_idx, topk_w, status_word};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (const cudaError_t ge = cudaGetDevice(&dev); ge != cudaSuccess) return from_cuda(ge);
     const bool tc_ok = route_tc_supported(a, dev);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (algo == MOE_ROUTE_TCGEN05 && !tc_ok) return MOE_ERR_UNSUPPORTED;
@@ -128,9 +135,7 @@ moe_status moe_route_stats(const void *X, const void *W_gate, const float *bias,
     if ((lse && !aligned4(lse)) || (expert_counts && !aligned4(expert_counts))) return MOE_ERR_MISALIGNED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (N == 0) {
-        if (expert_counts && cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        return MOE_OK;
+        return expert_counts ? from_cuda(cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s)) : MOE_OK;
     }
     if (!X || !W_gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
     if (H % 8 != 0) return MOE_ERR_MISALIGNED;
@@ -142,12 +147,14 @@ moe_status moe_route_stats(const void *X, const void *W_gate, const float *bias,
     a.lse = lse;
     a.counts = expert_counts;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (const cudaError_t ge = cudaGetDevice(&dev); ge != cudaSuccess) return from_cuda(ge);
     const bool tc_ok = route_tc_supported(a, dev);
     if (algo == MOE_ROUTE_TCGEN05 && !tc_ok) return MOE_ERR_UNSUPPORTED;
     // the kernels add their selections to the counts
-    if (expert_counts && cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (expert_counts) {
+        const moe_status ms = from_cuda(cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s));
+        if (ms != MOE_OK) return ms;
+    }
     if (algo == MOE_ROUTE_SIMT || !tc_ok) return from_cuda(launch_route_simt(a, s));
     return from_cuda(launch_route_tc(a, s));
 }
@@ -225,9 +232,9 @@ moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, in
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (N == 0) {
         // no tokens: every count and offset is zero
-        if (cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
-        if (cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
-        return MOE_OK;
+        cudaError_t me = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s);
+        if (me == cudaSuccess) me = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s);
+        return from_cuda(me);
     }
     if (use_ws) {
         // Large row copies run as a second launch: the permute kernel keeps up to
@@ -242,14 +249,14 @@ moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, in
             if (!copy_apart) return MOE_OK;
             return from_cuda(launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, ue8m0, status_word, s));
         }
-        if (f != cudaErrorNotSupported) return MOE_ERR_CUDA;
+        if (f != cudaErrorNotSupported) return from_cuda(f);
     }
     cudaError_t e = launch_dispatch_meta(topk_idx, N, E, K, expert_counts, expert_offsets, row_map, src_slot,
                                          status_word, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (e != cudaSuccess) return from_cuda(e);
     if (X) {
         e = launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, ue8m0, status_word, s);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        if (e != cudaSuccess) return from_cuda(e);
     }
     return MOE_OK;
 }
