@@ -113,23 +113,22 @@ extern "C" MOE_API moe_status moe_dispatch_ep(const int32_t *topk_idx, const voi
     const int R = ep_size;
     const int P = E / R;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (const cudaError_t ge = cudaGetDevice(&dev); ge != cudaSuccess) return from_cuda(ge);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (N == 0) {
-        if (cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
-            cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess ||
-            cudaMemsetAsync(rank_counts, 0, sizeof(int32_t) * R, s) != cudaSuccess ||
-            cudaMemsetAsync(rank_offsets, 0, sizeof(int32_t) * (R + 1), s) != cudaSuccess ||
-            cudaMemsetAsync(send_meta, 0, sizeof(int32_t) * R * (P + 1), s) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        return MOE_OK;
+        cudaError_t me = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s);
+        if (me == cudaSuccess) me = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s);
+        if (me == cudaSuccess) me = cudaMemsetAsync(rank_counts, 0, sizeof(int32_t) * R, s);
+        if (me == cudaSuccess) me = cudaMemsetAsync(rank_offsets, 0, sizeof(int32_t) * (R + 1), s);
+        if (me == cudaSuccess) me = cudaMemsetAsync(send_meta, 0, sizeof(int32_t) * R * (P + 1), s);
+        return from_cuda(me);
     }
     if (!dispatch_fused_supported(N, K, dev)) return MOE_ERR_UNSUPPORTED;
     // 1. experts as keys, metadata only; the inverse map goes to expand_idx
     cudaError_t e = launch_dispatch_fused(topk_idx, nullptr, N, 0, E, K, expert_counts, expert_offsets, row_map,
                                           expand_idx, nullptr, nullptr, nullptr, 0, status_word, workspace,
                                           workspace_bytes, s, 0);
-    if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+    if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : from_cuda(e);
     // 2. EP ranks as keys with deduplication; the first slot of each send row goes to send_token.
     // A large send-row copy runs as its own permute launch (more warps storing), before the
     // fix-up fills in the slots that take no row of their own
@@ -138,10 +137,10 @@ extern "C" MOE_API moe_status moe_dispatch_ep(const int32_t *topk_idx, const voi
     e = launch_dispatch_fused(topk_idx, copy_apart ? nullptr : X, N, X ? H : 0, R, K, rank_counts, rank_offsets,
                               slot_send_row, send_token, X_send, nullptr, nullptr, 0, status_word, workspace,
                               workspace_bytes, s, P);
-    if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+    if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : from_cuda(e);
     if (copy_apart) {
         e = launch_permute(X, slot_send_row, N, H, K, X_send, nullptr, nullptr, 0, status_word, s, true);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        if (e != cudaSuccess) return from_cuda(e);
     }
     // 3. fix-up
     const int sms = device_sm_count(dev);
@@ -159,5 +158,5 @@ extern "C" MOE_API moe_status moe_dispatch_ep(const int32_t *topk_idx, const voi
                            static_cast<const int32_t *>(expert_offsets), static_cast<const int32_t *>(rank_counts),
                            static_cast<const int32_t *>(rank_offsets), slot_send_row, send_token, expand_idx,
                            send_meta);
-    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return from_cuda(e);
 }

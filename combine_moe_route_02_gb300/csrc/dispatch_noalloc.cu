@@ -66,7 +66,7 @@ extern "C" MOE_API moe_status moe_dispatch_noalloc(const int32_t *topk_idx, cons
         return moe_dispatch(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map, src_slot, X_perm, X_fp8,
                             X_scale, status_word, nullptr, 0, stream);
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (const cudaError_t ge = cudaGetDevice(&dev); ge != cudaSuccess) return from_cuda(ge);
     // Sizes beyond what the built-in scratch serves: one launch takes at most
     // one CTA per SM and 16384 slots per CTA.
     const int64_t sms = device_sm_count(dev);
@@ -79,7 +79,7 @@ extern "C" MOE_API moe_status moe_dispatch_noalloc(const int32_t *topk_idx, cons
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents: the grid-barrier counters
     // must start at zero, the per-CTA counts are overwritten before use.
-    if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (const cudaError_t me = cudaMemsetAsync(scratch, 0, 256, s); me != cudaSuccess) return from_cuda(me);
     return moe_dispatch(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map, src_slot, X_perm, X_fp8,
                         X_scale, status_word, scratch, kScratchBytes, s);
 }

@@ -16,15 +16,6 @@ std::atomic<int> g_cc_major[kMaxDevices];
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// A failed launch is reported by the status alone: the runtime's last-error slot
-// is cleared so that a caller's later, unrelated check does not see it again.
-inline moe_status from_cuda(cudaError_t e)
-{
-    if (e == cudaSuccess) return MOE_OK;
-    (void)cudaGetLastError();
-    return MOE_ERR_CUDA;
-}
-
 moe_status check_topk(int E, int K)
 {
     if (E < 1 || E > 256) return MOE_ERR_INVALID_ARG;

@@ -329,6 +329,16 @@ struct NvtxRange {
     NvtxRange &operator=(const NvtxRange &) = delete;
 };
 
+// The status of a CUDA runtime call for the C ABI.  A failure is reported by the
+// status alone: the runtime's last-error slot is cleared so that a caller's
+// later, unrelated check does not see it again.
+inline moe_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return MOE_OK;
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+}
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count(int device);
 int device_cc_major(int device);
