@@ -83,6 +83,7 @@ struct TcParams {
     uint32_t win_off;      // byte offset of the per-token winning logits
     uint32_t staging_off;  // split mode: byte offset of the DSMEM staging area
     uint32_t tail_off;     // byte offset of TcSmemTail
+    int staging_alias;     // split mode: the staging area overlays the TMA ring
 };
 
 // Row stride (floats) of the split-mode staging buffer: NP + 4 keeps rows
@@ -271,9 +272,11 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
     tc_fence_before_sync();
     __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after_sync();
-    // split mode: announce that this CTA runs (peers wait for it before writing
-    // into its shared memory); the matching wait comes after the MMAs
-    if constexpr (SPLIT) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    // split mode with a staging area of its own: announce that this CTA runs
+    // (peers wait for it before writing into its shared memory); the matching
+    // wait comes after the MMAs
+    if constexpr (SPLIT)
+        if (!p.staging_alias) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const uint32_t tmem_base = tail.tmem_base;
     // inputs may come from the previous kernel in the stream (programmatic launch)
     pdl_wait_prior_grids();
@@ -496,8 +499,10 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
         const int RS = stage_row_floats(p.NP);
         float *buf = reinterpret_cast<float *>(smem + p.staging_off);  // [S slices][R rows][RS]
         __syncwarp();
-        // every CTA of the cluster has started, so its staging area may be written
-        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+        if (p.staging_alias)
+            cluster_sync_all();  // every CTA's MMAs are complete, so its ring may be overwritten
+        else  // every CTA of the cluster has started, so its staging area may be written
+            asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
         if (warp >= 2 && acc_ok && nkb > 0) {
             const int q = warp & 3;
             const int h = (warp - 2) >> 2;
@@ -654,10 +659,10 @@ int kmax_for(int K) { return K <= 2 ? 2 : K <= 4 ? 4 : K <= 8 ? 8 : 16; }
 
 constexpr size_t kSmemLimit = 227 * 1024;
 
-// Layout of a launch's shared memory: 1 KiB alignment slack, the TMA ring (or,
-// if larger, the split staging area), the exchange area, the tail and the bias.
+// Layout of a launch's shared memory.
 struct TcLayout {
     int stages;
+    bool alias;
     uint32_t exch_off, win_off, staging_off, tail_off;
     size_t smem;
 };
@@ -665,31 +670,52 @@ struct TcLayout {
 // Shared memory of a launch: 1 KiB alignment slack, the TMA ring, then
 // (split mode) the DSMEM staging area, the epilogue exchange area, the tail
 // and the bias.  Split CTAs run only kb_per K-steps, so their ring needs no
-// more stages than that; they prefer to fit two CTAs per SM.
-bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, TcLayout &L)
+// more stages than that; they prefer to fit two CTAs per SM.  With alias set
+// the staging area overlays the ring instead (it is written only once every
+// CTA of the cluster has finished its MMAs), for gates so wide that a ring
+// beside it would hold a single stage.
+bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, TcLayout &L)
 {
     const size_t slot = kABytes + static_cast<size_t>(EP) * kBK * 2;
     const size_t staging = split ? static_cast<size_t>(kBM) * stage_row_floats(NP) * sizeof(float) : 0;
+    const size_t apart = alias ? 0 : staging;
     const size_t exch = (split ? 0 : exch_lists_bytes(kmax)) + win_bytes(kmax);
-    const size_t fixed = 1024 + staging + exch + sizeof(TcSmemTail) + (sizeof(float) + sizeof(int)) * EP;
+    const size_t fixed = 1024 + apart + exch + sizeof(TcSmemTail) + (sizeof(float) + sizeof(int)) * EP;
     const int max_st = split ? (kb_per < kMaxStages ? (kb_per < 1 ? 1 : kb_per) : kMaxStages) : kMaxStages;
     const int min_st = split ? 1 : 2;
     const size_t budgets[2] = {split ? static_cast<size_t>(113 * 1024) : kSmemLimit, kSmemLimit};
     for (size_t budget : budgets) {
         for (int st = max_st; st >= min_st; --st) {
-            const size_t ring = (static_cast<size_t>(st) * slot + 1023) & ~size_t(1023);
+            size_t ring = static_cast<size_t>(st) * slot;
+            if (alias && ring < staging) ring = staging;
+            ring = (ring + 1023) & ~size_t(1023);
             if (fixed + ring <= budget) {
                 L.stages = st;
-                L.staging_off = static_cast<uint32_t>(ring);
-                L.exch_off = static_cast<uint32_t>(ring + staging);
-                L.win_off = static_cast<uint32_t>(ring + staging + (split ? 0 : exch_lists_bytes(kmax)));
-                L.tail_off = static_cast<uint32_t>(ring + staging + exch);
+                L.alias = alias && split;
+                L.staging_off = static_cast<uint32_t>(alias ? 0 : ring);
+                L.exch_off = static_cast<uint32_t>(ring + apart);
+                L.win_off = static_cast<uint32_t>(ring + apart + (split ? 0 : exch_lists_bytes(kmax)));
+                L.tail_off = static_cast<uint32_t>(ring + apart + exch);
                 L.smem = fixed + ring;
                 return true;
             }
         }
     }
     return false;
+}
+
+// Split-mode layout: the staging area apart from the ring unless that leaves
+// a one-stage ring for more than one K-step and the overlay does better.
+bool split_layout(int EP, int NP, int kmax, int kb_per, TcLayout &L)
+{
+    const bool ok = layout_for(EP, NP, kmax, true, kb_per, false, L);
+    if (ok && (L.stages > 1 || kb_per <= 1)) return true;
+    TcLayout A;
+    if (layout_for(EP, NP, kmax, true, kb_per, true, A) && (!ok || A.stages > L.stages)) {
+        L = A;
+        return true;
+    }
+    return ok;
 }
 
 template <int KMAX, bool SPLIT>
@@ -767,17 +793,20 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
         if ((err = set_smem_attr<KMAX, true>(dev)) != cudaSuccess) return err;
         // every cluster must be resident at once (one wave), else use a smaller split
         for (; S > 1; S >>= 1) {
-            if (!layout_for(q.EP, q.NP, KMAX, true, (nk + S - 1) / S, L)) continue;
+            if (!split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, L)) continue;
             if (max_active_clusters<KMAX>(L.smem, S, dev) >= q.tiles) break;
         }
     }
     const bool split = S > 1;
-    if (!layout_for(q.EP, q.NP, KMAX, split, (nk + S - 1) / S, L)) return cudaErrorInvalidConfiguration;
+    if (split ? !split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, L)
+              : !layout_for(q.EP, q.NP, KMAX, false, nk, false, L))
+        return cudaErrorInvalidConfiguration;
     q.stages = L.stages;
     q.exch_off = L.exch_off;
     q.win_off = L.win_off;
     q.staging_off = L.staging_off;
     q.tail_off = L.tail_off;
+    q.staging_alias = L.alias ? 1 : 0;
     q.nsplit = S;
     q.kb_per = (nk + S - 1) / S;
     uint32_t cols = 32;
