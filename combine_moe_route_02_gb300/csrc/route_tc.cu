@@ -217,9 +217,11 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                                                                const TcParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte alignment for the 128-byte swizzle atoms
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte alignment for the 128-byte swizzle atoms, as an offset from the
+    // shared array: a pointer derived this way keeps its shared address space,
+    // so the compiler emits shared-memory loads and stores rather than generic ones
+    const uint32_t smem_pad = (1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u;
+    unsigned char *smem = smem_raw + smem_pad;
     const uint32_t b_slot_bytes = static_cast<uint32_t>(p.EP) * kBK * 2;
     unsigned char *a_base = smem;
     unsigned char *b_base = smem + static_cast<size_t>(p.stages) * kABytes;
@@ -540,34 +542,67 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
             const int part = t % G;
             const int n = first_tile * kBM + static_cast<int>(rank) * R + lrow;
             const int nslices = min(S, (nk + p.kb_per - 1) / p.kb_per);  // CTAs that had K-steps
-            int bk[KMAX], bi[KMAX];
-            topk_clear<KMAX>(bk, bi);
             const float *rowbuf = buf + lrow * RS;
+            const int sstride = R * RS;                 // floats between the slices of a row
+            // this thread's columns part, part + G, ...: eight per step with the loads
+            // issued first, alternately into two lists (each sees increasing ids)
+            int ak[KMAX], ai[KMAX], bk[KMAX], bi[KMAX];
+            topk_clear<KMAX>(ak, ai);
+            topk_clear<KMAX>(bk, bi);
+            int col = part;
 #pragma unroll 1
-            for (int col = part; col < E; col += G) {
+            for (; col + 7 * G < E; col += 8 * G) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)   // summed in slice order
+                    if (c < nslices) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) x[u] += rowbuf[c * sstride + col + u * G];
+                    }
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) {
+                    topk_push<KMAX>(ak, ai, order_key(logit_of(x[u], bias_s[col + u * G])), col + u * G);
+                    // (K > 8: one list, to stay within the registers of two CTAs per SM)
+                    if constexpr (KMAX <= 8)
+                        topk_push<KMAX>(bk, bi, order_key(logit_of(x[u + 1], bias_s[col + (u + 1) * G])),
+                                        col + (u + 1) * G);
+                    else
+                        topk_push<KMAX>(ak, ai, order_key(logit_of(x[u + 1], bias_s[col + (u + 1) * G])),
+                                        col + (u + 1) * G);
+                }
+            }
+#pragma unroll 1
+            for (; col < E; col += G) {
                 float x = 0.f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)   // independent loads, summed in slice order
-                    if (c < nslices) x += rowbuf[c * R * RS + col];
-                topk_push<KMAX>(bk, bi, order_key(logit_of(x, bias_s[col])), col);
+                for (int c = 0; c < 8; ++c)
+                    if (c < nslices) x += rowbuf[c * sstride + col];
+                topk_push<KMAX>(ak, ai, order_key(logit_of(x, bias_s[col])), col);
             }
-            // K rounds of selection across the G threads of the token (warp shuffles)
+            // K rounds of selection across the 2G lists of the token (warp shuffles
+            // between its G threads); the winner's list drops its head
             float *wrow = win_v + lrow;
             float m = 0.f;
 #pragma unroll 1
             for (int k = 0; k < K; ++k) {
-                int v = bk[0];
-                int i = bi[0];
-#pragma unroll 1
-                for (int o = G >> 1; o > 0; o >>= 1) {
-                    const int ov = __shfl_xor_sync(0xffffffffu, v, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-                    const bool up = ranks_above(ov, oi, v, i);
-                    v = up ? ov : v;
-                    i = up ? oi : i;
+                const bool from_b = ranks_above(bk[0], bi[0], ak[0], ai[0]);
+                int v = from_b ? bk[0] : ak[0];
+                int i = from_b ? bi[0] : ai[0];
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) {
+                    if (o < G) {
+                        const int ov = __shfl_xor_sync(0xffffffffu, v, o);
+                        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+                        const bool up = ranks_above(ov, oi, v, i);
+                        v = up ? ov : v;
+                        i = up ? oi : i;
+                    }
                 }
                 const float fv = key_value(v);
                 if (k == 0) m = fv;
+                topk_pop_if<KMAX>(ak, ai, ai[0] == i);
                 topk_pop_if<KMAX>(bk, bi, bi[0] == i);
                 if (part == 0) {
                     wrow[k * kBM] = fv;
