@@ -78,6 +78,7 @@ struct TcParams {
     int N, H, E, K, renorm;
     int need_z;            // the full softmax denominator is needed (renorm off, or lse requested)
     int EP, NP, stages, nsplit, kb_per, tiles;
+    int tile_rows;         // tokens per tile (kBM, or fewer so that the tiles fill whole waves of SMs)
     uint32_t tmem_cols;
     uint32_t exch_off;     // byte offset of the epilogue exchange area (from the aligned base)
     uint32_t win_off;      // byte offset of the per-token winning logits
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
             uint32_t g = 0;  // K-steps issued so far (across tiles)
             bool stop = false;
             for (int tile = first_tile; tile < p.tiles && !stop; tile += tile_step) {
-                const int m0 = tile * kBM;
+                const int m0 = tile * p.tile_rows;
                 for (int i = 0; i < nkb; ++i) {
                     const uint32_t s = g % p.stages;
                     const uint32_t use = g / p.stages;
@@ -445,7 +446,9 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                 named_barrier_sync(1 + q, 64);   // both halves' lists are ready
                 if (h == 0) {
                     // ---- two-way merge of the halves, K rounds; ids written as selected
-                    const int n = tile * kBM + row;
+                    const int n = tile * p.tile_rows + row;
+                    // rows past tile_rows belong to the next tile (the TMA box is kBM rows)
+                    const bool mine = row < p.tile_rows && n < p.N;
                     const int *ok = lst_k + KMAX * kBM + row;
                     const int *oi = lst_i + KMAX * kBM + row;
                     float *wrow = win_v + row;
@@ -459,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                         const bool take_b = ranks_above(kb, ib, ka, ia);
                         wrow[k * kBM] = key_value(take_b ? kb : ka);
                         const int sel = take_b ? ib : ia;
-                        if (n < p.N) {
+                        if (mine) {
                             p.topk_idx[static_cast<int64_t>(n) * K + k] = sel;
                             if (p.counts && sel < E) atomicAdd(hist_s + sel, 1);
                         }
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
 #pragma unroll 1
                         for (int k = 0; k < K; ++k) denom += expf(wrow[k * kBM] - m);
                     }
-                    if (n < p.N) {
+                    if (mine) {
 #pragma unroll 1
                         for (int k = 0; k < K; ++k)
                             p.topk_w[static_cast<int64_t>(n) * K + k] = expf(wrow[k * kBM] - m) / denom;
@@ -540,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
             const int G = (32 * kEpiWarps) / R;         // threads per token: 2S (4, 8 or 16)
             const int lrow = t / G;
             const int part = t % G;
-            const int n = first_tile * kBM + static_cast<int>(rank) * R + lrow;
+            const int n = first_tile * p.tile_rows + static_cast<int>(rank) * R + lrow;
             const int nslices = min(S, (nk + p.kb_per - 1) / p.kb_per);  // CTAs that had K-steps
             const float *rowbuf = buf + lrow * RS;
             const int sstride = R * RS;                 // floats between the slices of a row
@@ -833,6 +836,18 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
         }
     }
     const bool split = S > 1;
+    // persistent mode: tiles of fewer than kBM tokens where that lets every SM
+    // take the same number of tiles (each still loads a kBM-row box; the rows
+    // past its own are the next tile's, read from L2 a second time)
+    q.tile_rows = kBM;
+    if (!split) {
+        const int64_t waves = (q.tiles + sms - 1) / sms;
+        const int64_t rows = (a.N + waves * sms - 1) / (waves * sms);
+        if (rows >= 8 && rows < kBM) {
+            q.tile_rows = static_cast<int>(rows);
+            q.tiles = static_cast<int>((a.N + rows - 1) / rows);
+        }
+    }
     if (split ? !split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, L)
               : !layout_for(q.EP, q.NP, KMAX, false, nk, false, L))
         return cudaErrorInvalidConfiguration;
