@@ -63,6 +63,8 @@ def parse_args():
                    help="E4M3 block-scale output of fp8 workloads: fp32 scales or UE8M0 exponent bytes")
     p.add_argument("--ep-size", type=int, default=0,
                    help="dispatch as moe_dispatch_ep with this many EP ranks (dedup'd send rows, expand_idx)")
+    p.add_argument("--apart", action="store_true",
+                   help="route and dispatch as two calls even where moe_route_dispatch runs them as one launch")
     p.add_argument("--residual", action="store_true",
                    help="combine with the residual connection (forward_aggregate: moe_combine_residual)")
     return p.parse_args()
@@ -75,7 +77,8 @@ def dist_env():
     return rank, world, local
 
 
-KERNEL_SOURCES = {"route": "route_tc.cu", "dispatch": "dispatch.cu", "combine": "combine.cu"}
+KERNEL_SOURCES = {"route": "route_tc.cu", "dispatch": "dispatch.cu", "combine": "combine.cu",
+                  "route_dispatch": "route_tc.cu"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
 
@@ -148,7 +151,10 @@ def kernel_bytes(w: mi.Workload, residual: bool = False, ue8m0: bool = False, ep
         # send_token, read X once and write one row per (token, rank)
         return {"route": route, "dispatch": N * K * 4 * 4 + ep_rows * 4 + N * 2 * H + ep_rows * 2 * H,
                 "combine": combine}
-    return {"route": route, "dispatch": meta + permute, "combine": combine}
+    # route + dispatch in one launch: X is read once by the algorithm (the row copy
+    # takes it again from L2)
+    return {"route": route, "dispatch": meta + permute, "combine": combine,
+            "route_dispatch": route + meta + permute - N * 2 * H}
 
 
 # ----------------------------------------------------------------- clocks during the timed region
@@ -356,6 +362,10 @@ def combine_config(args):
         c["route"] = "moe_route_stats (logsumexp + expert histogram) and moe_load_stats every step"
     if mi.WORKLOADS[args.workload].fp8:
         c["fp8_scales"] = args.scale_format
+    if not (args.apart or args.ep_size or args.route_stats or mi.WORKLOADS[args.workload].fp8):
+        c["calls"] = "moe_route_dispatch (route + dispatch + row copy, one launch where split-K) + moe_combine"
+    else:
+        c["calls"] = "moe_route, moe_dispatch, moe_combine"
     return c
 
 
@@ -415,6 +425,9 @@ def run_ours(args, rank, world, local):
     cnt_buf = torch.empty(E, dtype=torch.int32, device=dev) if args.route_stats else None
     stats_buf = torch.empty(4, dtype=torch.float32, device=dev) if args.route_stats else None
     comb_fn = L.moe_combine if R is None else L.moe_combine_residual
+    # route and dispatch as one call (one launch where the router runs split-K)
+    fuse = not (args.apart or args.ep_size or args.route_stats or w.fp8)
+    fused_launches = ctypes.c_int(0)
 
     def call_args(xd, o, spp, wsp):
         """Arguments of the three C-ABI calls of one step: tokens from xd, output to o, on stream spp."""
@@ -435,25 +448,42 @@ def run_ours(args, rank, world, local):
             ca = (vp(Y), vp(d.row_map), vp(tw), N, H, K, vp(o), vp(st), spp)
         else:
             ca = (vp(Y), vp(d.row_map), vp(tw), vp(R), N, H, K, vp(o), vp(st), spp)
-        return ra, da, ca
+        fa = (vp(xd), vp(Wd), vp(bd), N, H, E, K, int(w.renorm), vp(idx), vp(tw), vp(d.expert_counts),
+              vp(d.expert_offsets), vp(d.row_map), vp(d.src_slot), vp(d.X_perm), vp(st), vp(wsp), wsp.numel(),
+              ctypes.byref(fused_launches), spp)
+        return ra, da, ca, fa
 
-    route_args, disp_args, comb_args = call_args(Xd, out, sp, ws)
-
-    def step(ev=None):
-        rc = 0
-        if ev is not None:
-            ev[0].record(stream)
-        rc |= route_fn(*route_args)
-        if ev is not None:
-            ev[1].record(stream)
-        rc |= disp_fn(*disp_args)                  # counting sort + row permute (+ E4M3), one launch
-        if ev is not None:
-            ev[2].record(stream)
-        rc |= comb_fn(*comb_args)
+    def issue(a, spp):
+        """The C-ABI calls of one step on stream spp; returns the OR of their status codes."""
+        ra, da, ca, fa = a
+        if fuse:
+            return L.moe_route_dispatch(*fa) | comb_fn(*ca)
+        rc = route_fn(*ra) | disp_fn(*da) | comb_fn(*ca)
         if stats_buf is not None:          # load statistics of the step (one small kernel)
+            rc |= L.moe_load_stats(vp(cnt_buf), E, vp(lse_buf), N, ctypes.c_float(1e-3), vp(stats_buf), spp)
+        return rc
+
+    step_args = call_args(Xd, out, sp, ws)
+    route_args, disp_args, comb_args, fused_args = step_args
+
+    def step():
+        rc = issue(step_args, sp)
+        if rc:
+            raise RuntimeError(f"a library call failed: {moe.status_string(rc)}")
+
+    def step_calls_timed(ev, fused):
+        """One step with an event pair around each call: [route, dispatch, combine], or
+        [route_dispatch, combine] for the one-launch call."""
+        rc = 0
+        calls = ([lambda: L.moe_route_dispatch(*fused_args)] if fused else
+                 [lambda: route_fn(*route_args), lambda: disp_fn(*disp_args)])
+        calls.append(lambda: comb_fn(*comb_args))
+        for j, c in enumerate(calls):
+            ev[j].record(stream)
+            rc |= c()
+        if stats_buf is not None and not fused:
             rc |= L.moe_load_stats(vp(cnt_buf), E, vp(lse_buf), N, ctypes.c_float(1e-3), vp(stats_buf), sp)
-        if ev is not None:
-            ev[3].record(stream)
+        ev[len(calls)].record(stream)
         if rc:
             raise RuntimeError(f"a library call failed: {moe.status_string(rc)}")
 
@@ -472,6 +502,8 @@ def run_ours(args, rank, world, local):
         step()
     torch.cuda.synchronize()
     assert st.item() == 0, moe.status_string(st.item())
+    if fuse:   # kernels of the one route + dispatch call (1 when fused), then the combine
+        kernels_per_step = fused_launches.value + 1
 
     # ---- timed region: K whole steps, each bracketed by an event pair (the L2
     # flush in between is outside the brackets; no events between the kernels
@@ -507,13 +539,20 @@ def run_ours(args, rank, world, local):
     kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ksteps)]
     for i in range(ksteps):
         flush.zero_()
-        step(kevs[i])
+        step_calls_timed(kevs[i], False)
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(ksteps)] if fuse else []
+    for i in range(len(fevs)):
+        flush.zero_()
+        step_calls_timed(fevs[i], True)
     torch.cuda.synchronize()
     if sampler:
         time.sleep(0.2)
         sampler.stop()
     t2 = time.time()
     per = {n: [ev[j].elapsed_time(ev[j + 1]) for ev in kevs] for j, n in enumerate(names)}
+    if fuse:
+        per["route_dispatch"] = [ev[0].elapsed_time(ev[1]) for ev in fevs]
+        per["combine_after_route_dispatch"] = [ev[1].elapsed_time(ev[2]) for ev in fevs]
 
     # ---- the same step replayed from a CUDA graph (launch overhead removed)
     graph = None
@@ -521,15 +560,15 @@ def run_ours(args, rank, world, local):
         gs = torch.cuda.Stream()
         gsp = ctypes.c_void_p(gs.cuda_stream)
         g_ws = moe.dispatch_workspace(E, dev, gs)
-        g_route, g_disp, g_comb = call_args(Xd, out, gsp, g_ws)
+        g_args = call_args(Xd, out, gsp, g_ws)
         gs.wait_stream(stream)
         with torch.cuda.stream(gs):
             for _ in range(2):  # warm the graph stream's workspace and plans
-                route_fn(*g_route); disp_fn(*g_disp); comb_fn(*g_comb)
+                issue(g_args, gsp)
         torch.cuda.synchronize()
         cg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg, stream=gs):
-            rc = route_fn(*g_route) | disp_fn(*g_disp) | comb_fn(*g_comb)
+            rc = issue(g_args, gsp)
         if rc:
             raise RuntimeError(moe.status_string(rc))
         gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ksteps)]
@@ -573,11 +612,7 @@ def run_ours(args, rank, world, local):
             cs.wait_event(ev_h[b])
             if i >= 2:
                 cs.wait_event(ev_d[b])              # Ob[b] of step i-2 has been read back
-            ra, da, ca = cargs[b]
-            rc = route_fn(*ra) | disp_fn(*da) | comb_fn(*ca)
-            if stats_buf is not None:
-                rc |= L.moe_load_stats(vp(cnt_buf), E, vp(lse_buf), N, ctypes.c_float(1e-3), vp(stats_buf),
-                                       ctypes.c_void_p(cs.cuda_stream))
+            rc = issue(cargs[b], ctypes.c_void_p(cs.cuda_stream))
             if rc:
                 raise RuntimeError("a library call failed")
             ev_c[b].record(cs)
@@ -648,11 +683,17 @@ def run_ours(args, rank, world, local):
     peak, peak_src = measured_peaks()
     kb = kernel_bytes(w, args.residual, args.scale_format == "ue8m0", ep_rows)
     kern = {}
-    for n in names:
+    for n in names + (["route_dispatch"] if fuse else []):
         ms = statistics.fmean(per[n])
         kern[n] = {"ms": ms, "algorithmic_bytes": kb[n], "gbs": kb[n] / (ms * 1e-3) / 1e9,
                    "frac_of_" + peak_src + "_hbm": kb[n] / (ms * 1e-3) / 1e9 / peak}
-    dom = max(names, key=lambda n: kern[n]["ms"])
+    if fuse:
+        kern["route_dispatch"]["launches"] = fused_launches.value
+        kern["combine_after_route_dispatch_ms"] = statistics.fmean(per["combine_after_route_dispatch"])
+    # the roofline is that of the longest kernel of the timed step (the route +
+    # dispatch call counts as a kernel only where it was one launch)
+    step_kernels = ["route_dispatch", "combine"] if fuse and fused_launches.value == 1 else names
+    dom = max(step_kernels, key=lambda n: kern[n]["ms"])
     roof = {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
             "frac": kern[dom]["gbs"] / peak, "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
             if peak_src == "measured" else "fallback 6800 GB/s",
@@ -680,7 +721,8 @@ def run_ours(args, rank, world, local):
         "load": {"max_over_mean": load[0], "p95_over_mean": load[1], "mean_slots_per_expert": load[3]},
         "torch_naive": naive,
         "timing": ("value: K steps, one event pair per step; kernels: a second pass of min(K,1000) "
-                   "steps with an event pair per call"),
+                   "steps with an event pair per call (route, dispatch and combine as separate calls; "
+                   "route_dispatch: the one call the step makes when fused)"),
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, residual=args.residual,

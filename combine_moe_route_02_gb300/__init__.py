@@ -22,7 +22,7 @@ from . import _build
 __all__ = [
     "build", "lib", "MoeError", "route", "route_stats", "load_stats", "dispatch", "dispatch_ep", "permute",
     "combine", "dispatch_workspace_size", "dispatch_workspace", "status_string", "ROUTE_AUTO", "ROUTE_TCGEN05",
-    "ROUTE_SIMT", "SCALE_FP32", "SCALE_UE8M0", "Dispatch", "DispatchEP",
+    "ROUTE_SIMT", "SCALE_FP32", "SCALE_UE8M0", "Dispatch", "DispatchEP", "route_dispatch",
 ]
 
 MOE_OK = 0
@@ -44,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "moe_route", "moe_route_ex", "moe_dispatch_workspace_size", "moe_dispatch",
     "moe_permute", "moe_combine", "moe_status_string", "moe_abi_version", "moe_dispatch_noalloc",
     "moe_combine_residual", "moe_dispatch_ex", "moe_permute_ex", "moe_route_stats", "moe_load_stats",
-    "moe_dispatch_ep",
+    "moe_dispatch_ep", "moe_route_dispatch",
 )
 
 SCALE_FP32, SCALE_UE8M0 = 0, 1
@@ -109,6 +109,9 @@ def lib():
     L.moe_dispatch_ex.restype = I32
     L.moe_permute_ex.argtypes = [P, P, I64, I32, I32, P, P, P, I32, P, P]
     L.moe_permute_ex.restype = I32
+    L.moe_route_dispatch.argtypes = [P, P, P, I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, SZ,
+                                     ctypes.POINTER(ctypes.c_int), P]
+    L.moe_route_dispatch.restype = I32
     L.moe_status_string.argtypes = [I32]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_abi_version.argtypes = []
@@ -298,6 +301,46 @@ def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, f
         _ptr(status), _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
     _check(code, "moe_dispatch_ex")
     return out
+
+
+def route_dispatch(X: torch.Tensor, W_gate: torch.Tensor, K: int, bias: Optional[torch.Tensor] = None,
+                   renorm: bool = True, permute: bool = True, want_src_slot: bool = True, topk_idx=None,
+                   topk_w=None, out: Optional[Dispatch] = None, workspace: Optional[torch.Tensor] = None,
+                   status=None, stream=None):
+    """Router, then the counting-sort dispatch of its ids with a bf16 row copy
+    (moe_route_dispatch): one launch where the router runs split-K, else the two
+    calls.  Returns (topk_idx, topk_w, Dispatch, kernels launched)."""
+    N, H = X.shape
+    E = W_gate.shape[1]
+    _need(X, "X", torch.bfloat16)
+    _need(W_gate, "W_gate", torch.bfloat16, (H, E))
+    if bias is not None:
+        _need(bias, "bias", torch.float32, (E,))
+    dev = X.device
+    if topk_idx is None:
+        topk_idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((N, K), dtype=torch.float32, device=dev)
+    _need(topk_idx, "topk_idx", torch.int32, (N, K))
+    _need(topk_w, "topk_w", torch.float32, (N, K))
+    if out is None:
+        out = Dispatch(
+            expert_counts=torch.empty(E, dtype=torch.int32, device=dev),
+            expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            row_map=torch.empty(N * K, dtype=torch.int32, device=dev),
+            src_slot=torch.empty(N * K, dtype=torch.int32, device=dev) if want_src_slot else None,
+            X_perm=torch.empty((N * K, H), dtype=torch.bfloat16, device=dev) if permute else None,
+        )
+    if workspace is None:
+        workspace = dispatch_workspace(E, dev, stream)
+    launches = ctypes.c_int(0)
+    code = lib().moe_route_dispatch(
+        _ptr(X), _ptr(W_gate), _ptr(bias), N, H, E, K, int(bool(renorm)), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(out.expert_counts), _ptr(out.expert_offsets), _ptr(out.row_map), _ptr(out.src_slot),
+        _ptr(out.X_perm), _ptr(status), _ptr(workspace), workspace.numel(), ctypes.byref(launches),
+        _stream(stream))
+    _check(code, "moe_route_dispatch")
+    return topk_idx, topk_w, out, launches.value
 
 
 @dataclass

@@ -52,20 +52,6 @@ __device__ __forceinline__ void cluster_wait_acquire()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Lanes of the warp whose key equals this lane's key, for keys in [0, 512):
-// one ballot per key bit, all independent (cheaper here than __match_any_sync).
-__device__ __forceinline__ uint32_t same_key_lanes(int key)
-{
-    uint32_t m = 0xffffffffu;
-#pragma unroll
-    for (int b = 0; b < 9; ++b) {
-        const bool bit = (key >> b) & 1;
-        const uint32_t bal = __ballot_sync(0xffffffffu, bit);
-        m &= bit ? bal : ~bal;
-    }
-    return m;
-}
-
 __device__ __forceinline__ int ld_dsmem_i32(const int *local_ptr, uint32_t cta)
 {
     uint32_t remote;
@@ -460,18 +446,6 @@ struct FusedParams {
     int32_t *hist;  // [gridDim.x][E]
     int ep_P;       // 0: keys are the expert ids; > 0: keys are EP ranks (E of them, ep_P experts each)
 };
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void red_add_release_gpu(unsigned *p, unsigned v)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 struct FusedSmem {
     int total[kMaxE];       // grid-wide count per expert

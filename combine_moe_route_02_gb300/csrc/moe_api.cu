@@ -194,12 +194,15 @@ static moe_status validate_permute(const void *X, const int32_t *row_map, int64_
     return MOE_OK;
 }
 
-moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
-                           int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
-                           void *X_perm, void *X_fp8, void *X_scale, int scale_format, int32_t *status_word,
-                           void *workspace, size_t workspace_bytes, moe_stream_t stream)
+}  // extern "C"
+
+// moe_dispatch_ex; *launches receives the number of kernels launched.
+static moe_status dispatch_impl(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                                int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
+                                void *X_perm, void *X_fp8, void *X_scale, int scale_format, int32_t *status_word,
+                                void *workspace, size_t workspace_bytes, cudaStream_t s, int *launches)
 {
-    NvtxRange nvtx_range("moe_dispatch");
+    *launches = 0;
     moe_status st = check_topk(E, K);
     if (st != MOE_OK) return st;
     if ((st = check_rows(N, K)) != MOE_OK) return st;
@@ -220,7 +223,6 @@ moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, in
             return st;
     }
     const int ue8m0 = scale_format == MOE_SCALE_UE8M0;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (N == 0) {
         // no tokens: every count and offset is zero
         cudaError_t me = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s);
@@ -237,7 +239,9 @@ moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, in
                                                     expert_offsets, row_map, src_slot, X_perm, X_fp8, X_scale, ue8m0,
                                                     status_word, workspace, workspace_bytes, s);
         if (f == cudaSuccess) {
+            *launches = 1;
             if (!copy_apart) return MOE_OK;
+            *launches = 2;
             return from_cuda(launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, ue8m0, status_word, s));
         }
         if (f != cudaErrorNotSupported) return from_cuda(f);
@@ -245,11 +249,76 @@ moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, in
     cudaError_t e = launch_dispatch_meta(topk_idx, N, E, K, expert_counts, expert_offsets, row_map, src_slot,
                                          status_word, s);
     if (e != cudaSuccess) return from_cuda(e);
+    *launches = 1;
     if (X) {
         e = launch_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, ue8m0, status_word, s);
         if (e != cudaSuccess) return from_cuda(e);
+        *launches = 2;
     }
     return MOE_OK;
+}
+
+extern "C" {
+
+moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                           int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
+                           void *X_perm, void *X_fp8, void *X_scale, int scale_format, int32_t *status_word,
+                           void *workspace, size_t workspace_bytes, moe_stream_t stream)
+{
+    NvtxRange nvtx_range("moe_dispatch");
+    int launches = 0;
+    return dispatch_impl(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map, src_slot, X_perm, X_fp8,
+                         X_scale, scale_format, status_word, workspace, workspace_bytes,
+                         reinterpret_cast<cudaStream_t>(stream), &launches);
+}
+
+moe_status moe_route_dispatch(const void *X, const void *W_gate, const float *bias, int64_t N, int H, int E, int K,
+                              int renorm, int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                              int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot, void *X_perm,
+                              int32_t *status_word, void *workspace, size_t workspace_bytes, int *launches,
+                              moe_stream_t stream)
+{
+    NvtxRange nvtx_range("moe_route_dispatch");
+    if (launches) *launches = 0;
+    moe_status st = check_topk(E, K);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(N, K)) != MOE_OK) return st;
+    if (H < 1) return MOE_ERR_INVALID_ARG;
+    if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < moe_dispatch_workspace_size(N, E, K)) return MOE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MOE_ERR_MISALIGNED;
+    if (!aligned4(expert_counts) || !aligned4(expert_offsets) || (status_word && !aligned4(status_word)))
+        return MOE_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        cudaError_t me = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s);
+        if (me == cudaSuccess) me = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s);
+        return from_cuda(me);
+    }
+    if (!X || !W_gate || !topk_idx || !topk_w || !row_map) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_MISALIGNED;
+    if (!aligned16(X) || !aligned16(W_gate) || !aligned4(topk_idx) || !aligned4(topk_w) || !aligned4(row_map) ||
+        (bias && !aligned4(bias)) || (src_slot && !aligned4(src_slot)) || (X_perm && !aligned16(X_perm)))
+        return MOE_ERR_MISALIGNED;
+
+    RouteArgs a{X, W_gate, bias, N, H, E, K, renorm ? 1 : 0, topk_idx, topk_w, status_word};
+    FuseArgs f{expert_counts, expert_offsets, row_map, src_slot, X_perm, workspace};
+    const cudaError_t fe = launch_route_dispatch_tc(a, f, s);
+    if (fe == cudaSuccess) {
+        if (launches) *launches = 1;
+        return MOE_OK;
+    }
+    if (fe != cudaErrorNotSupported) return from_cuda(fe);
+    // apart: the router, then the dispatch of its ids
+    if ((st = moe_route_ex(X, W_gate, bias, N, H, E, K, renorm, topk_idx, topk_w, status_word, MOE_ROUTE_AUTO,
+                           stream)) != MOE_OK)
+        return st;
+    int disp = 0;
+    st = dispatch_impl(topk_idx, X_perm ? X : nullptr, N, H, E, K, expert_counts, expert_offsets, row_map,
+                       src_slot, X_perm, nullptr, nullptr, MOE_SCALE_FP32, status_word, workspace, workspace_bytes,
+                       s, &disp);
+    if (launches) *launches = 1 + disp;
+    return st;
 }
 
 moe_status moe_dispatch(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,

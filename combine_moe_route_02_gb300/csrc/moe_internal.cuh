@@ -37,6 +37,33 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Lanes of the warp whose key equals this lane's key, for keys in [0, 512):
+// one ballot per key bit, all independent (cheaper here than __match_any_sync).
+__device__ __forceinline__ uint32_t same_key_lanes(int key)
+{
+    uint32_t m = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < 9; ++b) {
+        const bool bit = (key >> b) & 1;
+        const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+
+// Grid-barrier counters in global memory (acquire load, release add).
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_add_release_gpu(unsigned *p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
@@ -115,6 +142,20 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(cache_policy)
         : "memory");
 }
+
+// Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple
+// of 16), completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
@@ -284,8 +325,19 @@ struct RouteArgs {
     int32_t *counts = nullptr;   // [E] selections per expert, accumulated (zeroed first), or nullptr
 };
 
+// Outputs of the dispatch part of a route + dispatch launch.
+struct FuseArgs {
+    int32_t *counts, *offsets, *row_map, *src_slot;
+    void *X_perm;      // bf16 rows in expert order, or nullptr (metadata only)
+    void *workspace;   // fused_workspace_bytes(E) bytes, 256-byte aligned, barrier counters zero
+};
+
 // Whether the tensor-core router can take this shape on the current device.
 bool route_tc_supported(const RouteArgs &a, int device);
+// Route and dispatch in one cooperative launch (split-mode router, every CTA
+// resident).  cudaErrorNotSupported when this shape or device cannot take it;
+// nothing has been launched then.
+cudaError_t launch_route_dispatch_tc(const RouteArgs &a, const FuseArgs &f, cudaStream_t stream);
 cudaError_t launch_route_tc(const RouteArgs &a, cudaStream_t stream);
 cudaError_t launch_route_simt(const RouteArgs &a, cudaStream_t stream);
 

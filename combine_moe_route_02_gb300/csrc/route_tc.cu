@@ -53,6 +53,9 @@ constexpr int kBM = 128;                       // tokens per tile (UMMA M)
 constexpr int kBK = 64;                        // bf16 per 128-byte swizzle row (one K-step)
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // 320
+constexpr int kWarps = kThreads / 32;
+constexpr int kFuseMaxCtas = 1024;   // rows of the per-CTA count table in the dispatch workspace
+constexpr int64_t kFuseMaxCopyBytes = 32ll << 20;   // fused row copies up to this size
 constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KiB X tile per slot
 constexpr uint32_t kBBoxBytes = kBK * 64 * 2;  // 8 KiB per 64-expert gate box
 constexpr int kMaxStages = 12;
@@ -85,6 +88,15 @@ struct TcParams {
     uint32_t staging_off;  // split mode: byte offset of the DSMEM staging area
     uint32_t tail_off;     // byte offset of TcSmemTail
     int staging_alias;     // split mode: the staging area overlays the TMA ring
+    // route + dispatch in one launch (split mode, every CTA resident): the counting
+    // sort of the launch's slots and the bf16 row copy after a grid barrier
+    int32_t *d_counts, *d_offsets, *d_row_map, *d_src_slot;
+    const uint4 *d_X;      // X as 16-byte chunks
+    uint4 *d_Xp;           // [N*K, H] bf16 rows in expert order, or nullptr
+    unsigned *d_bar;       // [0] arrive, [1] depart: zero before the launch, returned to zero
+    int32_t *d_hist;       // [CTAs][E] slot count per CTA and expert
+    int d_prefetch;        // the CTA's X rows are bulk-copied to shared memory offset 0 first
+    uint32_t d_scr_off;    // byte offset of the dispatch scratch (an mbarrier, then the counts)
 };
 
 // Row stride (floats) of the split-mode staging buffer: NP + 4 keeps rows
@@ -212,7 +224,233 @@ __device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float a, float b, flo
                  : "memory");
 }
 
-template <int KMAX, bool SPLIT>
+// Dispatch of a split-mode launch's own tokens, run by all threads of every CTA
+// once its top-K ids are in global memory: CTA c = tile * S + rank owns tokens
+// [c R, c R + R) (R = kBM / S), so the CTAs in index order hold the slots in
+// token order.  Per-warp ballot histograms give each slot its rank among the
+// CTA's slots of the same expert (stable in slot order); the CTA's counts go to
+// the grid-wide table, a bounded grid barrier follows, then every CTA sums the
+// table (all CTAs: expert totals; lower CTAs: rows before its own), forms the
+// exclusive prefix, writes row_map (and src_slot), and copies its tokens' rows
+// into X_perm.  `scr` is shared memory no longer in use (the staging area).
+template <int KMAX>
+__device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned char *smem)
+{
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int E = p.E;
+    const int K = p.K;
+    const int S = p.nsplit;
+    const int R = kBM / S;
+    const int c = static_cast<int>(blockIdx.y) * S + static_cast<int>(blockIdx.x);
+    const unsigned G = gridDim.x * gridDim.y;
+    const int64_t n0 = static_cast<int64_t>(c) * R;
+    const int64_t left = p.N - n0;
+    const int ntok = left <= 0 ? 0 : (left < R ? static_cast<int>(left) : R);
+    const int ns = ntok * K;
+    const int64_t s0 = n0 * K;
+    uint64_t *pf_bar = reinterpret_cast<uint64_t *>(smem + p.d_scr_off);
+    int *wcnt = reinterpret_cast<int *>(smem + p.d_scr_off + 16);   // [kWarps][E]
+    int *total = wcnt + kWarps * E;    // [E]
+    int *before = total + E;           // [E]
+    int *offset = before + E;          // [E + 1]
+    int *rows_s = offset + E + 1;      // [ns]
+    int *flag = rows_s + R * K;        // [1]
+    const int per_warp = (ns + kWarps - 1) / kWarps;
+    const int w0 = min(ns, per_warp * warp);
+    const int w1 = min(ns, w0 + per_warp);
+    int *my_cnt = wcnt + warp * E;
+
+    const int chunks = p.H >> 3;
+    const bool pf = p.d_prefetch && p.d_Xp != nullptr && ntok > 0;
+    // the rows this CTA will copy do not depend on the dispatch: start their
+    // bulk copy into shared memory now (the router is done with all of it)
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (pf && tid == 0) {
+        mbar_init(pf_bar, 1);
+        fence_mbarrier_init();
+        mbar_arrive_expect_tx(pf_bar, static_cast<uint32_t>(ntok) * chunks * 16u);
+        bulk_load(smem, p.d_X + n0 * chunks, static_cast<uint32_t>(ntok) * chunks * 16u, pf_bar);  // rows are contiguous
+    }
+    for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+    for (int e = tid; e < E; e += kThreads) {
+        total[e] = 0;
+        before[e] = 0;
+    }
+    __syncthreads();
+    // per-warp histograms of contiguous slot ranges (ids written by this CTA
+    // before the last block-wide barrier)
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        int e = i < w1 ? p.topk_idx[s0 + i] : E;
+        if (e < 0 || e >= E) e = E;
+        const uint32_t peers = same_key_lanes(e);
+        if (e < E && lane == __ffs(peers) - 1) my_cnt[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) {
+        int run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const int v = wcnt[w * E + e];
+            wcnt[w * E + e] = run;
+            run += v;
+        }
+        p.d_hist[static_cast<int64_t>(c) * E + e] = run;
+    }
+
+    // grid barrier (bounded): every CTA arrives, whatever happened before
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        red_add_release_gpu(&p.d_bar[0], 1u);
+        const uint64_t tb = globaltimer_ns();
+        int ok = 1;
+        for (uint32_t it = 0; ld_acquire_gpu(&p.d_bar[0]) < G; ++it) {
+            if ((it & 255u) == 255u && globaltimer_ns() - tb > kWaitLimitNs) {
+                ok = 0;
+                break;
+            }
+        }
+        *flag = ok;
+    }
+    __syncthreads();
+    if (!*flag) {
+        if (tid == 0) report_status(p.status, MOE_ERR_TIMEOUT);
+        if (pf) {   // let the row copy land before the CTA exits
+            volatile int no_abort = 0;
+            mbar_wait_bounded(pf_bar, 0, &no_abort);
+        }
+        return;
+    }
+
+    // expert totals and the rows of lower CTAs: thread (grp, e) sums table rows
+    // grp, grp + groups, ...; sixteen loads in flight before the first add
+    {
+        const int groups = kThreads / E;   // >= 1 (E <= 256)
+        const int e = tid % E;
+        const int grp = tid / E;
+        if (grp < groups) {
+            int tot = 0, bef = 0;
+            for (int c0 = grp; c0 < static_cast<int>(G); c0 += 16 * groups) {
+                int v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int cc = c0 + u * groups;
+                    v[u] = cc < static_cast<int>(G) ? __ldcg(p.d_hist + static_cast<int64_t>(cc) * E + e) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    tot += v[u];
+                    bef += (c0 + u * groups < c) ? v[u] : 0;
+                }
+            }
+            atomicAdd(&total[e], tot);
+            atomicAdd(&before[e], bef);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive prefix over the experts, eight per lane
+        int vals[8];
+        int local = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            vals[i] = e < E ? total[e] : 0;
+            local += vals[i];
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        int run = incl - local;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            if (e < E) offset[e] = run;
+            run += vals[i];
+        }
+        if (lane == 31) offset[E] = incl;
+    }
+    __syncthreads();
+    if (c == 0) {
+        for (int e = tid; e <= E; e += kThreads) {
+            p.d_offsets[e] = offset[e];
+            if (e < E) p.d_counts[e] = total[e];
+        }
+    }
+    for (int i = tid; i < kWarps * E; i += kThreads) {
+        const int e = i % E;
+        wcnt[i] += offset[e] + before[e];
+    }
+    __syncthreads();
+
+    // stable scatter: slot i of this CTA gets row offset + before + its rank
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        int e = i < w1 ? p.topk_idx[s0 + i] : E;
+        if (e < 0 || e >= E) e = E;
+        const uint32_t peers = same_key_lanes(e);
+        const uint32_t below = peers & ((1u << lane) - 1u);
+        if (i < w1) {
+            const int r = e < E ? my_cnt[e] + __popc(below) : -1;
+            rows_s[i] = r;
+            p.d_row_map[s0 + i] = r;
+            if (e < E && p.d_src_slot) p.d_src_slot[r] = static_cast<int32_t>(s0 + i);
+        }
+        __syncwarp();
+        if (e < E && below == 0) my_cnt[e] += __popc(peers);
+        __syncwarp();
+    }
+
+    // the last CTA to leave returns the barrier counters to zero
+    if (tid == 0) {
+        const unsigned old = atomicAdd(&p.d_bar[1], 1u);
+        if (old == G - 1) {
+            p.d_bar[0] = 0;
+            p.d_bar[1] = 0;
+            __threadfence();
+        }
+    }
+
+    // rows of this CTA's tokens, one warp per token: from shared memory where
+    // they were prefetched, else from global memory (L2, where the router just
+    // streamed them)
+    if (p.d_Xp != nullptr) {
+        __syncthreads();
+        if (pf) {
+            // the copy depends on nothing but memory: wait for it (time-bounded)
+            // whatever else went wrong, so that no copy is in flight at exit
+            volatile int no_abort = 0;
+            if (!mbar_wait_bounded(pf_bar, 0, &no_abort)) {
+                if (tid == 0) report_status(p.status, MOE_ERR_TIMEOUT);
+                return;
+            }
+        }
+        const uint4 *rows = reinterpret_cast<const uint4 *>(smem);
+        for (int j = warp; j < ntok; j += kWarps) {
+            const uint4 *src = pf ? rows + static_cast<size_t>(j) * chunks : p.d_X + (n0 + j) * chunks;
+            int rk[KMAX];
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k) rk[k] = k < K ? rows_s[j * K + k] : -1;
+#pragma unroll 4
+            for (int ch = lane; ch < chunks; ch += 32) {
+                const uint4 v = pf ? src[ch] : __ldg(src + ch);
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k)
+                    if (rk[k] >= 0) p.d_Xp[static_cast<int64_t>(rk[k]) * chunks + ch] = v;
+            }
+        }
+    }
+    pdl_launch_dependents();
+}
+
+template <int KMAX, bool SPLIT, bool FUSE = false>
 __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                const __grid_constant__ CUtensorMap tmW,
                                                                const TcParams p)
@@ -271,7 +509,9 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
     }
     // One wave of CTAs: the next kernel in the stream may start launching now
     // (it still waits for this grid to complete before it reads anything).
-    pdl_launch_dependents();
+    // With the dispatch fused in, the trigger comes at the end instead: CTAs of
+    // the next kernel placed early would crowd onto the SMs this launch leaves free.
+    if constexpr (!FUSE) pdl_launch_dependents();
     tc_fence_before_sync();
     __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after_sync();
@@ -655,6 +895,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
     if (threadIdx.x == 0 && tail.abort) report_status(p.status, MOE_ERR_TIMEOUT);
+    if constexpr (FUSE) fused_dispatch_tail<KMAX>(p, smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -756,25 +997,26 @@ bool split_layout(int EP, int NP, int kmax, int kb_per, TcLayout &L)
     return ok;
 }
 
-template <int KMAX, bool SPLIT>
+template <int KMAX, bool SPLIT, bool FUSE = false>
 cudaError_t set_smem_attr(int dev)
 {
     static std::atomic<uint64_t> configured{0};
     const uint64_t bit = 1ull << (dev & 63);
     if (configured.load() & bit) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(route_tc_kernel<KMAX, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(route_tc_kernel<KMAX, SPLIT, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemLimit));
     if (err == cudaSuccess) configured.fetch_or(bit);
     return err;
 }
 
-template <int KMAX>
+template <int KMAX, bool FUSE = false>
 int max_active_clusters(size_t smem, int S, int dev)
 {
     // cached per (device, cluster size, shared memory size)
     static std::mutex mu;
     static std::map<uint64_t, int> cache;
-    const uint64_t key = (static_cast<uint64_t>(dev) << 40) | (static_cast<uint64_t>(S) << 32) | smem;
+    const uint64_t key = (static_cast<uint64_t>(FUSE) << 48) | (static_cast<uint64_t>(dev) << 40) |
+                         (static_cast<uint64_t>(S) << 32) | smem;
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -792,7 +1034,7 @@ int max_active_clusters(size_t smem, int S, int dev)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, route_tc_kernel<KMAX, true>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, route_tc_kernel<KMAX, true, FUSE>, &cfg) != cudaSuccess) n = 0;
     std::lock_guard<std::mutex> g(mu);
     cache[key] = n;
     return n;
@@ -800,7 +1042,7 @@ int max_active_clusters(size_t smem, int S, int dev)
 
 template <int KMAX>
 cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CUtensorMap &tmW, cudaStream_t stream,
-                            int dev)
+                            int dev, const FuseArgs *fz = nullptr)
 {
     const int sms = device_sm_count(dev);
     TcParams q;
@@ -810,6 +1052,14 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     q.status = a.status;
     q.lse = a.lse;
     q.counts = a.counts;
+    q.d_counts = fz ? fz->counts : nullptr;
+    q.d_offsets = fz ? fz->offsets : nullptr;
+    q.d_row_map = fz ? fz->row_map : nullptr;
+    q.d_src_slot = fz ? fz->src_slot : nullptr;
+    q.d_X = static_cast<const uint4 *>(a.X);
+    q.d_Xp = fz ? static_cast<uint4 *>(fz->X_perm) : nullptr;
+    q.d_bar = fz ? static_cast<unsigned *>(fz->workspace) : nullptr;
+    q.d_hist = fz ? reinterpret_cast<int32_t *>(static_cast<unsigned char *>(fz->workspace) + 256) : nullptr;
     q.N = static_cast<int>(a.N);
     q.H = a.H;
     q.E = a.E;
@@ -828,14 +1078,22 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     cudaError_t err;
     TcLayout L;
     if (S > 1) {
-        if ((err = set_smem_attr<KMAX, true>(dev)) != cudaSuccess) return err;
+        if ((err = fz ? set_smem_attr<KMAX, true, true>(dev) : set_smem_attr<KMAX, true>(dev)) != cudaSuccess)
+            return err;
         // every cluster must be resident at once (one wave), else use a smaller split
         for (; S > 1; S >>= 1) {
             if (!split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, L)) continue;
-            if (max_active_clusters<KMAX>(L.smem, S, dev) >= q.tiles) break;
+            const int fit = fz ? max_active_clusters<KMAX, true>(L.smem, S, dev)
+                               : max_active_clusters<KMAX>(L.smem, S, dev);
+            if (fit >= q.tiles) break;
         }
     }
     const bool split = S > 1;
+    // route + dispatch in one launch needs the split mode (one wave of CTAs); a
+    // large row copy is left to the dispatch kernel, which spreads it over every SM
+    if (fz && (!split || static_cast<int64_t>(S) * q.tiles > kFuseMaxCtas ||
+               (fz->X_perm != nullptr && a.N * a.K * 2 * static_cast<int64_t>(a.H) > kFuseMaxCopyBytes)))
+        return cudaErrorNotSupported;
     // persistent mode: tiles of fewer than kBM tokens where that lets every SM
     // take the same number of tiles (each still loads a kBM-row box; the rows
     // past its own are the next tile's, read from L2 a second time)
@@ -858,6 +1116,19 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     q.tail_off = L.tail_off;
     q.staging_alias = L.alias ? 1 : 0;
     q.nsplit = S;
+    q.d_prefetch = 0;
+    q.d_scr_off = L.staging_off;
+    if (fz) {
+        // the dispatch scratch: an mbarrier (16 bytes) and the counts; with room,
+        // the CTA's kBM / S rows of X are first copied to offset 0 of shared memory
+        const size_t R = static_cast<size_t>(kBM / S);
+        const size_t scratch = 16 + sizeof(int) * (13 * static_cast<size_t>(a.E) + 2 + R * a.K);
+        const size_t rows_bytes = (R * 2 * a.H + 15) & ~size_t(15);
+        if (fz->X_perm != nullptr && rows_bytes + scratch <= L.tail_off) {
+            q.d_prefetch = 1;
+            q.d_scr_off = static_cast<uint32_t>(rows_bytes);
+        }
+    }
     q.kb_per = (nk + S - 1) / S;
     uint32_t cols = 32;
     const uint32_t need = static_cast<uint32_t>(split ? q.NP : 2 * q.NP);  // persistent: two accumulators
@@ -865,7 +1136,7 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     q.tmem_cols = cols;
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     int na = 0;
     if (split) {
         cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(q.tiles), 1);
@@ -885,6 +1156,18 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     ++na;
     cfg.attrs = attr;
     cfg.numAttrs = na;
+    if (fz) {
+        // all CTAs resident at once: the grid barrier of the dispatch part cannot deadlock
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        cfg.numAttrs = na + 1;
+        err = cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, true, true>, tmX, tmW, q);
+        if (err != cudaSuccess) {
+            (void)cudaGetLastError();   // not launched: the caller routes and dispatches apart
+            return cudaErrorNotSupported;
+        }
+        return cudaSuccess;
+    }
     if (split) return cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, true>, tmX, tmW, q);
     if ((err = set_smem_attr<KMAX, false>(dev)) != cudaSuccess) return err;
     return cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, false>, tmX, tmW, q);
@@ -900,6 +1183,25 @@ bool route_tc_supported(const RouteArgs &a, int device)
     if (a.N > 0x7fffffff - kBM) return false;
     if (reinterpret_cast<uintptr_t>(a.X) % 16 || reinterpret_cast<uintptr_t>(a.W) % 16) return false;
     return encode_tiled_fn() != nullptr;
+}
+
+cudaError_t launch_route_dispatch_tc(const RouteArgs &a, const FuseArgs &f, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (!route_tc_supported(a, dev)) return cudaErrorNotSupported;
+    CUtensorMap tmX, tmW;
+    if (!encode_2d_bf16(&tmX, a.X, static_cast<uint64_t>(a.H), static_cast<uint64_t>(a.N), kBK, kBM))
+        return cudaErrorInvalidValue;
+    if (!encode_2d_bf16(&tmW, a.W, static_cast<uint64_t>(a.E), static_cast<uint64_t>(a.H), 64, kBK))
+        return cudaErrorInvalidValue;
+    switch (kmax_for(a.K)) {
+    case 2: return plan_and_launch<2>(a, tmX, tmW, stream, dev, &f);
+    case 4: return plan_and_launch<4>(a, tmX, tmW, stream, dev, &f);
+    case 8: return plan_and_launch<8>(a, tmX, tmW, stream, dev, &f);
+    default: return plan_and_launch<16>(a, tmX, tmW, stream, dev, &f);
+    }
 }
 
 cudaError_t launch_route_tc(const RouteArgs &a, cudaStream_t stream)

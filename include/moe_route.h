@@ -209,6 +209,35 @@ MOE_API moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X,
                            moe_stream_t stream);
 
 /*
+ * moe_route_dispatch -- moe_route_ex (MOE_ROUTE_AUTO) followed by
+ * moe_dispatch_ex of its own top-K ids with a bf16 row copy: the router of the
+ * moe-engine page (融合Triton路由内核) and the counting sort of the PithTrain
+ * page (§8.2), with the same outputs as the two calls.  Where the tensor-core
+ * router runs in its split-K mode (few tokens: every CTA resident at once) the
+ * whole path is ONE cooperative launch: each CTA, after its top-K epilogue,
+ * counts its own slots, a bounded grid barrier follows, and every CTA then
+ * forms the offsets, writes row_map for its slots and copies its tokens' rows
+ * (from L2, where the router just streamed them).  Otherwise, or where the
+ * cooperative launch is refused, the two calls run one after the other.
+ *   X, W_gate, bias, renorm, topk_idx, topk_w   as moe_route
+ *   expert_counts, expert_offsets, row_map, src_slot   as moe_dispatch
+ *   X_perm       bf16 [N*K, H], 16-byte aligned, or NULL (metadata only)
+ *   workspace    at least moe_dispatch_workspace_size(N, E, K) bytes, 256-byte
+ *                aligned, zero before the first call (left zero by every call
+ *                that did not time out)
+ *   launches     host int or NULL: out, the number of kernels this call launched
+ * Errors: those of moe_route_ex and moe_dispatch_ex; MOE_ERR_WORKSPACE when the
+ * workspace is missing or too small.
+ */
+MOE_API moe_status moe_route_dispatch(const void *X, const void *W_gate, const float *bias,
+                              int64_t N, int H, int E, int K, int renorm,
+                              int32_t *topk_idx, float *topk_w,
+                              int32_t *expert_counts, int32_t *expert_offsets,
+                              int32_t *row_map, int32_t *src_slot, void *X_perm,
+                              int32_t *status_word, void *workspace, size_t workspace_bytes,
+                              int *launches, moe_stream_t stream);
+
+/*
  * moe_dispatch_ep -- expert-parallel dispatch metadata with token
  * deduplication for the tokens of one GPU: the metadata of
  * fused_dedup_prepare_dispatch on the PithTrain page (§8.2 O(n) counting sort

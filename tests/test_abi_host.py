@@ -141,6 +141,34 @@ def test_permute_and_combine_validation(L):
     assert L.moe_combine_residual(A, A2, A3, R, 8, 64, 0, A4, None, None) == INVALID
 
 
+def route_dispatch(L, X=A, W=A2, N=16, H=64, E=16, K=2, idx=A3, w=A4, counts=A, offsets=A2, row_map=A3,
+                   src=None, xp=None, ws=0x100000, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = L.moe_dispatch_workspace_size(N, E, K)
+    n = ctypes.c_int(-1)
+    code = L.moe_route_dispatch(X, W, None, N, H, E, K, 1, idx, w, counts, offsets, row_map, src, xp, None, ws,
+                                ws_bytes, ctypes.byref(n), None)
+    assert n.value == 0          # nothing launched on a rejected call
+    return code
+
+
+def test_route_dispatch_validation(L):
+    assert route_dispatch(L, E=0) == INVALID
+    assert route_dispatch(L, K=17, E=32) == INVALID
+    assert route_dispatch(L, N=-1) == INVALID
+    assert route_dispatch(L, H=0) == INVALID
+    assert route_dispatch(L, counts=None) == INVALID
+    assert route_dispatch(L, ws=None) == WORKSPACE
+    assert route_dispatch(L, ws_bytes=64) == WORKSPACE
+    assert route_dispatch(L, ws=0x100000 + 16) == MISALIGNED
+    assert route_dispatch(L, X=None) == INVALID
+    assert route_dispatch(L, row_map=None) == INVALID
+    assert route_dispatch(L, H=12) == MISALIGNED
+    assert route_dispatch(L, X=A + 8) == MISALIGNED
+    assert route_dispatch(L, xp=A4 + 4) == MISALIGNED
+    assert route_dispatch(L, src=A + 2) == MISALIGNED
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
 def test_valid_call_without_gpu_fails_loudly(L):
     # arguments pass validation, then the first CUDA call fails: MOE_ERR_CUDA, no crash
@@ -148,6 +176,8 @@ def test_valid_call_without_gpu_fails_loudly(L):
     assert L.moe_combine(A, A2, A3, 8, 64, 2, A4, None, None) == CUDA
     assert L.moe_combine_residual(A, A2, A3, 0x50000, 8, 64, 2, A4, None, None) == CUDA
     assert L.moe_load_stats(A, 16, None, 0, ctypes.c_float(1e-3), A2, None) == CUDA
+    assert L.moe_route_dispatch(A, A2, None, 16, 64, 16, 2, 1, A3, A4, A, A2, A3, None, None, None, 0x100000,
+                                L.moe_dispatch_workspace_size(16, 16, 2), None, None) == CUDA
     # UE8M0 scale bytes need no alignment: the call passes validation (then fails on CUDA)
     assert L.moe_permute_ex(A, A2, 8, 128, 2, A3, A4, A + 2, 1, None, None) == CUDA
 

@@ -600,3 +600,74 @@ def test_graph_capture_replays_the_path():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+# ------------------------------------------------------------------ route + dispatch in one call
+
+# (N, H, E, K, bias+renorm off, launches with rows, launches metadata-only): split-mode
+# router shapes with a row copy of at most 32 MiB run as ONE launch; the others
+# route and then dispatch (the row copy in a launch of its own from 256 MiB)
+ROUTE_DISPATCH_CASES = [
+    (2048, 1024, 64, 2, False, 1, 1),     # the bench workload (clusters of 4)
+    (512, 256, 16, 2, False, 1, 1),
+    (4096, 512, 64, 4, False, 1, 1),
+    (4096, 2048, 64, 4, False, 2, 1),     # 64 MiB of rows: the dispatch kernel copies them
+    (777, 512, 32, 3, True, 1, 1),        # ragged last tile, bias, renorm off
+    (600, 2048, 256, 8, False, 1, 1),     # staging area overlaid on the TMA ring
+    (1000, 7168, 256, 8, False, 2, 1),
+    (130, 2048, 256, 16, False, 1, 1),    # K = 16
+    (9000, 256, 64, 2, False, 1, 1),      # 71 tiles, clusters of 2
+    (1, 64, 8, 1, False, 2, 2),           # one K-step: no split, router and dispatch apart
+    (16384, 2048, 128, 8, False, 3, 2),   # persistent router
+    (300, 128, 12, 3, False, 2, 2),       # E % 8 != 0: CUDA-core router
+]
+
+
+@pytest.mark.parametrize("permute", [True, False])
+@pytest.mark.parametrize("N,H,E,K,skew,launches,launches_meta", ROUTE_DISPATCH_CASES)
+def test_route_dispatch_matches_oracle(N, H, E, K, skew, launches, launches_meta, permute):
+    X, W, bias = mi.make_route_inputs(N, H, E, N + H + K, skew=skew)
+    renorm = not skew
+    st = status_word()
+    idx, tw, d, n_launch = moe.route_dispatch(X.to(DEV), W.to(DEV), K, None if bias is None else bias.to(DEV),
+                                              renorm, permute=permute, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0, moe.status_string(st.item())
+    assert n_launch == (launches if permute else launches_meta)
+    r_idx, r_w, L, P = oracle_route(X, W, bias, K, renorm)
+    gi = idx.cpu().numpy()
+    compare_topk(gi, tw.cpu().numpy(), r_idx, r_w, L, P, renorm)
+    # the dispatch of the GPU's own ids: bit-exact against the oracle
+    c, o, r, s = oracle.dispatch(gi, E)
+    assert np.array_equal(d.expert_counts.cpu().numpy(), c)
+    assert np.array_equal(d.expert_offsets.cpu().numpy(), o)
+    assert np.array_equal(d.row_map.cpu().numpy(), r)
+    assert np.array_equal(d.src_slot.cpu().numpy(), s)
+    if permute:
+        assert np.array_equal(bits(d.X_perm), oracle.permute(bits(X), r, K))
+
+
+def test_route_dispatch_workspace_reused():
+    # the grid-barrier counters go back to zero after every call
+    N, H, E, K = 2048, 1024, 64, 2
+    ws = torch.zeros(moe.dispatch_workspace_size(N, E, K), dtype=torch.uint8, device=DEV)
+    st = status_word()
+    for seed in range(4):
+        X, W, _ = mi.make_route_inputs(N, H, E, seed)
+        idx, tw, d, n = moe.route_dispatch(X.to(DEV), W.to(DEV), K, workspace=ws, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0 and n == 1
+        assert int(ws[:8].view(torch.int32).abs().sum()) == 0
+        c, o, r, s = oracle.dispatch(idx.cpu().numpy(), E)
+        assert np.array_equal(d.row_map.cpu().numpy(), r)
+        assert np.array_equal(bits(d.X_perm), oracle.permute(bits(X), r, K))
+
+
+def test_route_dispatch_empty():
+    N, H, E, K = 0, 256, 16, 2
+    X = torch.empty((0, H), dtype=torch.bfloat16, device=DEV)
+    W = mi.random_bf16((H, E), seed=3).to(DEV)
+    idx, tw, d, n = moe.route_dispatch(X, W, K)
+    torch.cuda.synchronize()
+    assert n == 0
+    assert int(d.expert_counts.abs().sum()) == 0 and int(d.expert_offsets.abs().sum()) == 0
