@@ -153,6 +153,22 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
                  : "memory");
 }
 
+// Plain bulk copy shared -> global (16-byte aligned addresses, size a multiple
+// of 16), tracked in this thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+
+// Wait until every bulk copy this thread committed has completed (its reads of
+// shared memory and its writes to global memory).
+__device__ __forceinline__ void bulk_commit_and_wait_all()
+{
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Orders this thread's earlier generic-proxy accesses to shared memory before
 // later async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

@@ -418,9 +418,9 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
         }
     }
 
-    // rows of this CTA's tokens, one warp per token: from shared memory where
-    // they were prefetched, else from global memory (L2, where the router just
-    // streamed them)
+    // rows of this CTA's tokens: where they were prefetched, one bulk store per
+    // destination row (the TMA engine copies them out of shared memory); else one
+    // warp per token from global memory (L2, where the router just streamed them)
     if (p.d_Xp != nullptr) {
         __syncthreads();
         if (pf) {
@@ -431,19 +431,29 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
                 if (tid == 0) report_status(p.status, MOE_ERR_TIMEOUT);
                 return;
             }
-        }
-        const uint4 *rows = reinterpret_cast<const uint4 *>(smem);
-        for (int j = warp; j < ntok; j += kWarps) {
-            const uint4 *src = pf ? rows + static_cast<size_t>(j) * chunks : p.d_X + (n0 + j) * chunks;
-            int rk[KMAX];
+            bool issued = false;
+            for (int i = tid; i < ns; i += kThreads) {
+                const int r = rows_s[i];
+                if (r >= 0) {
+                    bulk_store(p.d_Xp + static_cast<int64_t>(r) * chunks, smem + static_cast<size_t>(i / K) * chunks * 16,
+                               static_cast<uint32_t>(chunks) * 16u);
+                    issued = true;
+                }
+            }
+            if (issued) bulk_commit_and_wait_all();
+        } else {
+            for (int j = warp; j < ntok; j += kWarps) {
+                const uint4 *src = p.d_X + (n0 + j) * chunks;
+                int rk[KMAX];
 #pragma unroll
-            for (int k = 0; k < KMAX; ++k) rk[k] = k < K ? rows_s[j * K + k] : -1;
+                for (int k = 0; k < KMAX; ++k) rk[k] = k < K ? rows_s[j * K + k] : -1;
 #pragma unroll 4
-            for (int ch = lane; ch < chunks; ch += 32) {
-                const uint4 v = pf ? src[ch] : __ldg(src + ch);
+                for (int ch = lane; ch < chunks; ch += 32) {
+                    const uint4 v = __ldg(src + ch);
 #pragma unroll
-                for (int k = 0; k < KMAX; ++k)
-                    if (rk[k] >= 0) p.d_Xp[static_cast<int64_t>(rk[k]) * chunks + ch] = v;
+                    for (int k = 0; k < KMAX; ++k)
+                        if (rk[k] >= 0) p.d_Xp[static_cast<int64_t>(rk[k]) * chunks + ch] = v;
+                }
             }
         }
     }
