@@ -485,6 +485,17 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if constexpr (SPLIT) {
+        // The split-K exchange writes into the shared memory of the other CTAs of
+        // the cluster: run only as planned, in clusters of nsplit CTAs (the same
+        // for every CTA, so all of them return together before any barrier)
+        uint32_t ncta;
+        asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
+        if (ncta != static_cast<uint32_t>(p.nsplit)) {
+            if (threadIdx.x == 0) report_status(p.status, MOE_ERR_UNSUPPORTED);
+            return;
+        }
+    }
     const uint32_t rank = SPLIT ? cluster_rank() : 0u;
     const int nk = (p.H + kBK - 1) / kBK;
     const int kb0 = SPLIT ? static_cast<int>(rank) * p.kb_per : 0;

@@ -227,7 +227,10 @@ MOE_API moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X,
  *                that did not time out)
  *   launches     host int or NULL: out, the number of kernels this call launched
  * Errors: those of moe_route_ex and moe_dispatch_ex; MOE_ERR_WORKSPACE when the
- * workspace is missing or too small.
+ * workspace is missing or too small.  The status word receives
+ * MOE_ERR_UNSUPPORTED (and no output is written) if a split-K launch did not
+ * run in clusters of the planned size, MOE_ERR_TIMEOUT if the grid barrier ran
+ * out (the workspace must then be zeroed before it is used again).
  */
 MOE_API moe_status moe_route_dispatch(const void *X, const void *W_gate, const float *bias,
                               int64_t N, int H, int E, int K, int renorm,
