@@ -686,7 +686,8 @@ def run_ours(args, rank, world, local):
     for n in names + (["route_dispatch"] if fuse else []):
         ms = statistics.fmean(per[n])
         kern[n] = {"ms": ms, "algorithmic_bytes": kb[n], "gbs": kb[n] / (ms * 1e-3) / 1e9,
-                   "frac_of_" + peak_src + "_hbm": kb[n] / (ms * 1e-3) / 1e9 / peak}
+                   "frac_of_" + peak_src + "_hbm": kb[n] / (ms * 1e-3) / 1e9 / peak,
+                   "traffic": ncu_traffic(n, w.name)}
     if fuse:
         kern["route_dispatch"]["launches"] = fused_launches.value
         kern["combine_after_route_dispatch_ms"] = statistics.fmean(per["combine_after_route_dispatch"])
