@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 import moe_inputs as mi  # noqa: E402
 
 METRIC = "route+dispatch+combine tokens/s on 1 GB300; % of HBM roofline per kernel"
+NOMINAL_HBM_GBS = 8000.0   # "about 8 TB/s": the nominal figure the per-kernel fractions are also quoted against
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 E2E_UNIT = 64          # pipelined end-to-end steps per CUDA graph
@@ -263,16 +264,42 @@ def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000, residual:
     r = oracle.run_path(Xb, Wb, b, w.K, w.renorm, w.fp8)   # untimed: provides the expert outputs Y
     Y = r["Y"]
     R = mi.bf16_bits(residual_rows(w)) if residual else None
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, ep_size, stats)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or reps >= max_reps:
-            break
-    return {"value": reps * w.N / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    def timed(limit_s):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, ep_size, stats)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= limit_s or reps >= max_reps:
+                return reps, el
+
+    cores = oracle.num_threads()
+    reps, el = timed(seconds)
+    # the same on one host thread, for a bounded sample (about half as long)
+    oracle.set_num_threads(1)
+    try:
+        reps1, el1 = timed(seconds / 2)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": reps * w.N / el, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"the whole {w.name} workload ({w.N} tokens), {reps} passes of route+dispatch+permute+"
-                      f"combine in fp64 C, {el:.1f} s"}
+                      f"combine in fp64 C, {el:.1f} s",
+            "single_thread": {"value": reps1 * w.N / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"{reps1} passes of the same, {el1:.1f} s"},
+            "cpu_model": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu prints it (else what the platform module knows)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
 
 
 def torch_naive(Xd, Wd, bd, w: mi.Workload, Y, flush, reps: int = 100):
@@ -544,7 +571,15 @@ def run_ours(args, rank, world, local):
     for i in range(len(fevs)):
         flush.zero_()
         step_calls_timed(fevs[i], True)
+    # ---- hot L2: the same steps with no flush in between (what fits in the
+    # 129 MB L2 stays there from one step to the next)
+    hevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ksteps)]
+    for i in range(ksteps):
+        hevs[i][0].record(stream)
+        step()
+        hevs[i][1].record(stream)
     torch.cuda.synchronize()
+    hot_ms = statistics.fmean(ev[0].elapsed_time(ev[1]) for ev in hevs)
     if sampler:
         time.sleep(0.2)
         sampler.stop()
@@ -685,8 +720,10 @@ def run_ours(args, rank, world, local):
     kern = {}
     for n in names + (["route_dispatch"] if fuse else []):
         ms = statistics.fmean(per[n])
-        kern[n] = {"ms": ms, "algorithmic_bytes": kb[n], "gbs": kb[n] / (ms * 1e-3) / 1e9,
+        kern[n] = {"ms": ms, "median_ms": statistics.median(per[n]), "algorithmic_bytes": kb[n],
+                   "gbs": kb[n] / (ms * 1e-3) / 1e9,
                    "frac_of_" + peak_src + "_hbm": kb[n] / (ms * 1e-3) / 1e9 / peak,
+                   "frac_of_nominal_8000": kb[n] / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
                    "traffic": ncu_traffic(n, w.name)}
     if fuse:
         kern["route_dispatch"]["launches"] = fused_launches.value
@@ -719,6 +756,12 @@ def run_ours(args, rank, world, local):
                         "latency_ms: one step alone, nothing overlapped, L2 flushed before"},
         "clocks": sampler.summary(t0, t2) if sampler else None,
         "graph": graph,
+        "hot_l2": {"ms_per_step": hot_ms, "tokens_per_s": N / (hot_ms * 1e-3), "steps": ksteps,
+                   "what": "the same step with no L2 flush between steps"},
+        "kernel_sum": {"tokens_per_s": N / (sum(kern[n]["median_ms"] for n in names) * 1e-3),
+                       "ms": sum(kern[n]["median_ms"] for n in names),
+                       "what": "N / (median route + median dispatch + median combine), each call timed alone "
+                               "with an event pair, L2 flushed before each step"},
         "load": {"max_over_mean": load[0], "p95_over_mean": load[1], "mean_slots_per_expert": load[3]},
         "torch_naive": naive,
         "timing": ("value: K steps, one event pair per step; kernels: a second pass of min(K,1000) "

@@ -77,6 +77,8 @@ def _load():
         lib.oracle_fp8_block_scale.argtypes = [ctypes.c_double]
         lib.oracle_fp8_block_scale.restype = ctypes.c_float
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
         return lib
 
@@ -103,6 +105,11 @@ def _check(rc, what):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's OpenMP loops from now on (the default is every host core)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def route(X_bits, W_bits, bias=None, K=1, renorm=True, want_logits=False, want_probs=False):

@@ -542,3 +542,20 @@ def test_whole_path_closed_form():
     ref = widen(mi.bf16_bits(X)) * f[:, None]
     out = widen(r["out"])
     assert np.all(np.abs(out - ref) <= 1e-2 * np.abs(ref) + 1e-30)
+
+
+def test_oracle_results_do_not_depend_on_thread_count():
+    # the CPU baseline times the oracle on every host core and on one; the results are the same
+    X, W, _ = mi.make_route_inputs(300, 128, 16, 7)
+    Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
+    n = oracle.num_threads()
+    try:
+        oracle.set_num_threads(1)
+        assert oracle.num_threads() == 1 or n == 1
+        one = oracle.run_path(Xb, Wb, None, 2)
+    finally:
+        oracle.set_num_threads(n)
+    assert oracle.num_threads() == n
+    many = oracle.run_path(Xb, Wb, None, 2)
+    for key in ("topk_idx", "topk_w", "row_map", "Xp", "out"):
+        assert np.array_equal(one[key], many[key]), key
