@@ -42,6 +42,7 @@ NOMINAL_HBM_GBS = 8000.0   # "about 8 TB/s": the nominal figure the per-kernel f
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 E2E_UNIT = 64          # pipelined end-to-end steps per CUDA graph
+E2E_BUFFERS = 2        # buffer sets of the pipelined end-to-end steps (3 or 4 measured no faster)
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -56,6 +57,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--e2e-buffers", type=int, default=E2E_BUFFERS, help="buffer sets of the pipelined e2e steps")
     p.add_argument("--no-torch-naive", action="store_true", help="skip the stock-PyTorch comparison figure")
     p.add_argument("--route-stats", action="store_true",
                    help="route with the router statistics (moe_route_stats: logsumexp + expert histogram) and "
@@ -619,34 +621,35 @@ def run_ours(args, rank, world, local):
         graph = {"error": str(exc)[:200]}
 
     # ---- end to end through the public API: every step uploads its tokens from
-    # pinned host memory and reads its output back.  Steps are pipelined over two
-    # buffer sets: the upload of step i+1 and the read-back of step i-1 run on
-    # their own streams while step i computes (the C-ABI calls go on the compute
-    # stream); the value is steps / elapsed time.  The serial latency of one
+    # pinned host memory and reads its output back.  Steps are pipelined over
+    # E2E_BUFFERS buffer sets: the upload of step i+1 and the read-back of step i-1
+    # run on their own streams while step i computes (the C-ABI calls go on the
+    # compute stream).  The value is steps / elapsed time.  The serial latency of one
     # step (upload, compute, read-back, nothing overlapped, L2 flushed before) is
     # reported beside it.
     Xh = X.pin_memory()
-    outh = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    NB = max(2, args.e2e_buffers)
+    outh = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(NB)]
     cs, hs, ds = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     c_ws = moe.dispatch_workspace(E, dev, cs)
-    Xb = [Xd, torch.empty_like(Xd)]
-    Ob = [out, torch.empty_like(out)]
-    cargs = [call_args(Xb[b], Ob[b], ctypes.c_void_p(cs.cuda_stream), c_ws) for b in range(2)]
-    ev_h = [torch.cuda.Event() for _ in range(2)]
-    ev_c = [torch.cuda.Event() for _ in range(2)]
-    ev_d = [torch.cuda.Event() for _ in range(2)]
+    Xb = [Xd] + [torch.empty_like(Xd) for _ in range(NB - 1)]
+    Ob = [out] + [torch.empty_like(out) for _ in range(NB - 1)]
+    cargs = [call_args(Xb[b], Ob[b], ctypes.c_void_p(cs.cuda_stream), c_ws) for b in range(NB)]
+    ev_h = [torch.cuda.Event() for _ in range(NB)]
+    ev_c = [torch.cuda.Event() for _ in range(NB)]
+    ev_d = [torch.cuda.Event() for _ in range(NB)]
 
     def pipelined(n):
         for i in range(n):
-            b = i & 1
-            if i >= 2:
-                hs.wait_event(ev_c[b])              # step i-2 has finished reading Xb[b]
+            b = i % NB
+            if i >= NB:
+                hs.wait_event(ev_c[b])              # step i-NB has finished reading Xb[b]
             with torch.cuda.stream(hs):
                 Xb[b].copy_(Xh, non_blocking=True)
             ev_h[b].record(hs)
             cs.wait_event(ev_h[b])
-            if i >= 2:
-                cs.wait_event(ev_d[b])              # Ob[b] of step i-2 has been read back
+            if i >= NB:
+                cs.wait_event(ev_d[b])              # Ob[b] of step i-NB has been read back
             rc = issue(cargs[b], ctypes.c_void_p(cs.cuda_stream))
             if rc:
                 raise RuntimeError("a library call failed")
@@ -656,7 +659,7 @@ def run_ours(args, rank, world, local):
                 outh[b].copy_(Ob[b], non_blocking=True)
             ev_d[b].record(ds)
 
-    pipelined(4)
+    pipelined(2 * NB)
     torch.cuda.synchronize()
     # The pipelined steps are issued two ways and both are timed: from the host
     # (one Python iteration per step) and as units of E2E_UNIT steps captured in
@@ -752,7 +755,7 @@ def run_ours(args, rank, world, local):
                 "issue": e2e_mode, "host_issued_ms_per_step": host_ms, "graph_ms_per_step": graph_ms,
                 "latency_ms": e2e_latency,
                 "path": "pinned host X -> device, route, dispatch, permute, combine, out -> pinned host, "
-                        "every step; steps pipelined over two buffer sets (copies on their own streams); "
+                        f"every step; steps pipelined over {NB} buffer sets (copies on their own streams); "
                         "latency_ms: one step alone, nothing overlapped, L2 flushed before"},
         "clocks": sampler.summary(t0, t2) if sampler else None,
         "graph": graph,
