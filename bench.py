@@ -122,6 +122,17 @@ def max_over_ranks(value: float, dist_mod=None, device=None) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(counts, dist_mod=None):
+    """The job-wide expert histogram: every rank's counts added up (an all-reduce of E
+    integers, for the load statistics only -- nothing on the data path exchanges tokens)."""
+    if dist_mod is None:
+        return counts
+    import torch
+    t = counts.to(torch.int64)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.SUM)
+    return t.to(counts.dtype)
+
+
 def weak_scaling_tokens_per_s(world: int, tokens_per_rank: int, steps: int, total_ms: float) -> float:
     """Whole-job throughput: every rank routes its own tokens_per_rank each step."""
     return world * tokens_per_rank * steps / (total_ms / 1e3)
@@ -712,11 +723,13 @@ def run_ours(args, rank, world, local):
         lat_ms.append(e0.elapsed_time(e1))
     e2e_latency = max_over_ranks(statistics.fmean(lat_ms), pg, dev)
 
+    # untimed: the expert counts of every rank's step added up, then moe_load_stats on them
+    job_counts = sum_over_ranks(d.expert_counts, pg)
     if rank != 0:
         pg.destroy_process_group()
         return
 
-    load = moe.load_stats(d.expert_counts).cpu().tolist()   # untimed: moe_load_stats on the step's counts
+    load = moe.load_stats(job_counts).cpu().tolist()
     naive = torch_naive(Xd, Wd, bd, w, Y, flush, reps=min(args.steps, 100)) if not args.no_torch_naive else None
     peak, peak_src = measured_peaks()
     kb = kernel_bytes(w, args.residual, args.scale_format == "ue8m0", ep_rows)
@@ -765,7 +778,8 @@ def run_ours(args, rank, world, local):
                        "ms": sum(kern[n]["median_ms"] for n in names),
                        "what": "N / (median route + median dispatch + median combine), each call timed alone "
                                "with an event pair, L2 flushed before each step"},
-        "load": {"max_over_mean": load[0], "p95_over_mean": load[1], "mean_slots_per_expert": load[3]},
+        "load": {"max_over_mean": load[0], "p95_over_mean": load[1], "mean_slots_per_expert": load[3],
+                 "over_ranks": world},
         "torch_naive": naive,
         "timing": ("value: K steps, one event pair per step; kernels: a second pass of min(K,1000) "
                    "steps with an event pair per call (route, dispatch and combine as separate calls; "
