@@ -671,3 +671,34 @@ def test_route_dispatch_empty():
     torch.cuda.synchronize()
     assert n == 0
     assert int(d.expert_counts.abs().sum()) == 0 and int(d.expert_offsets.abs().sum()) == 0
+
+
+def test_graph_capture_replays_route_dispatch():
+    # the one-launch route + dispatch (a cooperative cluster launch) inside a CUDA
+    # graph, then the combine; replays reproduce the eager results, on their own
+    # stream with their own workspace
+    w = mi.WORKLOADS["n2048_h1024_e64_k2"]
+    X, W, _ = mi.make_route_inputs(w.N, w.H, w.E, 5)
+    Xd, Wd = X.to(DEV), W.to(DEV)
+    idx, tw, d, n = moe.route_dispatch(Xd, Wd, w.K)
+    assert n == 1
+    Y = gpu_fixture(d.X_perm, d.expert_counts, w.E)
+    out = moe.combine(Y, d.row_map, tw)
+    torch.cuda.synchronize()
+    ref_out, ref_rows, ref_map = out.clone(), d.X_perm.clone(), d.row_map.clone()
+    s = torch.cuda.Stream()
+    ws = torch.zeros(moe.dispatch_workspace_size(w.N, w.E, w.K), dtype=torch.uint8, device=DEV)
+    st = status_word()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            moe.route_dispatch(Xd, Wd, w.K, topk_idx=idx, topk_w=tw, out=d, workspace=ws, status=st, stream=s)
+            moe.combine(Y, d.row_map, tw, out=out, status=st, stream=s)
+    for _ in range(3):
+        out.zero_()
+        d.X_perm.zero_()
+        d.row_map.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert st.item() == 0, moe.status_string(st.item())
+        assert torch.equal(out, ref_out) and torch.equal(d.X_perm, ref_rows) and torch.equal(d.row_map, ref_map)
