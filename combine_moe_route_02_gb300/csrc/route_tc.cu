@@ -232,7 +232,10 @@ __device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float a, float b, flo
 // the grid-wide table, a bounded grid barrier follows, then every CTA sums the
 // table (all CTAs: expert totals; lower CTAs: rows before its own), forms the
 // exclusive prefix, writes row_map (and src_slot), and copies its tokens' rows
-// into X_perm.  `scr` is shared memory no longer in use (the staging area).
+// into X_perm.  All of `smem` is free by then: with p.d_prefetch the CTA's rows
+// (contiguous in X) are bulk-copied to offset 0 before the barrier and leave as
+// one bulk store per destination row; the counts and an mbarrier live at
+// p.d_scr_off.
 template <int KMAX>
 __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned char *smem)
 {
