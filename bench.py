@@ -85,11 +85,35 @@ KERNEL_SOURCES = {"route": "route_tc.cu", "dispatch": "dispatch.cu", "combine": 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
 
+def code_only(text: str) -> str:
+    """C/CUDA source with comments removed and whitespace runs collapsed (string and
+    character literals kept), so that a digest changes with the code, not its comments."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_digest(kernel: str) -> str:
     import hashlib
     path = os.path.join(ROOT, "combine_moe_route_02_gb300", "csrc", KERNEL_SOURCES[kernel])
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path, encoding="utf-8") as f:
+        return hashlib.sha256(code_only(f.read()).encode()).hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):

@@ -71,3 +71,15 @@ def test_gpu_line_has_the_contract_keys():
     assert d["gpu_launches"] >= 2 * d["steps"]
     assert "route_dispatch" in d["kernels"] and d["kernels"]["route_dispatch"]["launches"] == 1
     assert d["roofline"]["kernel"] in ("route_dispatch", "combine")
+
+
+def test_source_digest_ignores_comments_only():
+    import bench
+    a = 'int f(int x) { // add one\n  return x + 1; /* done */ }\nconst char *s = "// kept";\n'
+    b = '/* header */\nint f(int x) {\n    return x + 1;\n}\nconst char *s = "// kept";  // trailing\n'
+    c = 'int f(int x) { return x + 2; }\nconst char *s = "// kept";\n'
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+    assert '"// kept"' in bench.code_only(a)
+    for k in ("route", "dispatch", "combine", "route_dispatch"):
+        assert len(bench.source_digest(k)) == 16
