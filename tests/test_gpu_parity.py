@@ -572,11 +572,13 @@ def test_workload_end_to_end(name):
 
 def test_workload_n4096_h2048_e64_k4_twenty_seeds():
     w = mi.WORKLOADS["n4096_h2048_e64_k4"]
-    total_mismatch = 0
+    total_mismatch = total_zone = 0
     for seed in w.seeds:
         s = check_workload(w, seed)
         total_mismatch += s["mismatched"]
-    print("n4096_h2048_e64_k4: seeds", len(w.seeds), "near-tie mismatches", total_mismatch)
+        total_zone += s["near_tie_zone"]
+    print("n4096_h2048_e64_k4: seeds", len(w.seeds), "tokens in the near-tie zone", total_zone,
+          "near-tie mismatches accepted", total_mismatch)
 
 
 def test_graph_capture_replays_the_path():
