@@ -418,6 +418,12 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def fused_step(args) -> bool:
+    """Whether the step makes route and dispatch one call (moe_route_dispatch): not for E4M3
+    output, the EP metadata, the router statistics, or when --apart asks for three calls."""
+    return not (args.apart or args.ep_size or args.route_stats or mi.WORKLOADS[args.workload].fp8)
+
+
 def combine_config(args):
     c = {"dispatch": f"moe_dispatch_ep, ep_size {args.ep_size}"} if args.ep_size else {}
     c["combine"] = ("forward_aggregate: weighted sum + residual, one bf16 rounding" if args.residual
@@ -426,7 +432,7 @@ def combine_config(args):
         c["route"] = "moe_route_stats (logsumexp + expert histogram) and moe_load_stats every step"
     if mi.WORKLOADS[args.workload].fp8:
         c["fp8_scales"] = args.scale_format
-    if not (args.apart or args.ep_size or args.route_stats or mi.WORKLOADS[args.workload].fp8):
+    if fused_step(args):
         c["calls"] = "moe_route_dispatch (route + dispatch + row copy, one launch where split-K) + moe_combine"
     else:
         c["calls"] = "moe_route, moe_dispatch, moe_combine"
@@ -490,7 +496,7 @@ def run_ours(args, rank, world, local):
     stats_buf = torch.empty(4, dtype=torch.float32, device=dev) if args.route_stats else None
     comb_fn = L.moe_combine if R is None else L.moe_combine_residual
     # route and dispatch as one call (one launch where the router runs split-K)
-    fuse = not (args.apart or args.ep_size or args.route_stats or w.fp8)
+    fuse = fused_step(args)
     fused_launches = ctypes.c_int(0)
 
     def call_args(xd, o, spp, wsp):
