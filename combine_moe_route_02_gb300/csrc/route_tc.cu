@@ -41,6 +41,8 @@
 #include <math.h>
 
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 
@@ -1181,10 +1183,17 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     cfg.attrs = attr;
     cfg.numAttrs = na;
     if (fz) {
-        // all CTAs resident at once: the grid barrier of the dispatch part cannot deadlock
+        // all CTAs resident at once: the grid barrier of the dispatch part cannot
+        // deadlock.  MOE_FUSED_LAUNCH=noncooperative drops the attribute (for
+        // profilers that run cooperative cluster launches without clusters); the
+        // one-wave check above still places every CTA at once on an idle GPU.
+        static const bool noncoop = [] {
+            const char *v = std::getenv("MOE_FUSED_LAUNCH");
+            return v != nullptr && std::strcmp(v, "noncooperative") == 0;
+        }();
         attr[na].id = cudaLaunchAttributeCooperative;
         attr[na].val.cooperative = 1;
-        cfg.numAttrs = na + 1;
+        cfg.numAttrs = noncoop ? na : na + 1;
         err = cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, true, true>, tmX, tmW, q);
         if (err != cudaSuccess) {
             (void)cudaGetLastError();   // not launched: the caller routes and dispatches apart

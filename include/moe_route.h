@@ -231,6 +231,11 @@ MOE_API moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X,
  * MOE_ERR_UNSUPPORTED (and no output is written) if a split-K launch did not
  * run in clusters of the planned size, MOE_ERR_TIMEOUT if the grid barrier ran
  * out (the workspace must then be zeroed before it is used again).
+ * The one launch is cooperative.  With the environment variable
+ * MOE_FUSED_LAUNCH=noncooperative (read once per process) it is launched
+ * without that attribute, for profilers that run cooperative cluster launches
+ * without clusters; every CTA is then still resident at once on an otherwise
+ * idle GPU (the launch is planned as one wave), but that is not guaranteed.
  */
 MOE_API moe_status moe_route_dispatch(const void *X, const void *W_gate, const float *bias,
                               int64_t N, int H, int E, int K, int renorm,
