@@ -704,3 +704,51 @@ def test_graph_capture_replays_route_dispatch():
         torch.cuda.synchronize()
         assert st.item() == 0, moe.status_string(st.item())
         assert torch.equal(out, ref_out) and torch.equal(d.X_perm, ref_rows) and torch.equal(d.row_map, ref_map)
+
+
+# ------------------------------------------------------------------ seeded random shapes
+
+def _random_shapes(count, seed=2026):
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for _ in range(count):
+        E = int(rng.choice([8, 16, 24, 32, 40, 64, 96, 128, 192, 256, 12, 7, 100]))
+        K = int(rng.integers(1, min(E, 16) + 1))
+        H = int(rng.choice([8, 64, 136, 256, 512, 1024, 2048]))
+        N = int(rng.choice([1, 3, 17, 129, 300, 1000, 2049, 5000]))
+        skew = bool(rng.integers(0, 2))
+        renorm = bool(rng.integers(0, 2))
+        shapes.append((N, H, E, K, skew, renorm))
+    return shapes
+
+
+@pytest.mark.parametrize("N,H,E,K,skew,renorm", _random_shapes(64))
+def test_random_shapes_whole_path_match_oracle(N, H, E, K, skew, renorm):
+    # route (auto implementation), dispatch with rows, route + dispatch as one call, and the
+    # combine, on shapes drawn across the supported range (E % 8 != 0 takes the CUDA-core router)
+    X, W, bias = mi.make_route_inputs(N, H, E, N * 7 + H + E + K, skew=skew)
+    Xd, Wd = X.to(DEV), W.to(DEV)
+    bd = None if bias is None else bias.to(DEV)
+    st = status_word()
+    idx, tw = moe.route(Xd, Wd, K, bd, renorm, status=st)
+    d = moe.dispatch(idx, E, Xd, status=st)
+    idx2, tw2, d2, _ = moe.route_dispatch(Xd, Wd, K, bd, renorm, status=st)
+    Y = gpu_fixture(d.X_perm, d.expert_counts, E)
+    out = moe.combine(Y, d.row_map, tw, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0, moe.status_string(st.item())
+    r_idx, r_w, L, P = oracle_route(X, W, bias, K, renorm)
+    # each path against the oracle on its own ids (the fused launch may split H differently,
+    # which changes the fp32 summation order of the logits)
+    for gidx, gw, dd in ((idx, tw, d), (idx2, tw2, d2)):
+        gi = gidx.cpu().numpy()
+        compare_topk(gi, gw.cpu().numpy(), r_idx, r_w, L, P, renorm)
+        c, o, r, s = oracle.dispatch(gi, E)
+        assert np.array_equal(dd.expert_counts.cpu().numpy(), c)
+        assert np.array_equal(dd.expert_offsets.cpu().numpy(), o)
+        assert np.array_equal(dd.row_map.cpu().numpy(), r)
+        assert np.array_equal(dd.src_slot.cpu().numpy(), s)
+        assert np.array_equal(bits(dd.X_perm), oracle.permute(bits(X), r, K))
+    _, _, r, _ = oracle.dispatch(idx.cpu().numpy(), E)
+    ref = oracle.combine(bits(Y), r, tw.cpu().numpy())
+    combine_close(bits(out), ref)
