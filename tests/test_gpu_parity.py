@@ -619,6 +619,7 @@ ROUTE_DISPATCH_CASES = [
     (1000, 7168, 256, 8, False, 2, 1),
     (130, 2048, 256, 16, False, 1, 1),    # K = 16
     (9000, 256, 64, 2, False, 1, 1),      # 71 tiles, clusters of 2
+    (300, 7168, 64, 2, False, 1, 1),      # a CTA's rows do not fit in shared memory: copied from L2
     (1, 64, 8, 1, False, 2, 2),           # one K-step: no split, router and dispatch apart
     (16384, 2048, 128, 8, False, 3, 2),   # persistent router
     (300, 128, 12, 3, False, 2, 2),       # E % 8 != 0: CUDA-core router
