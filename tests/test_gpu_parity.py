@@ -6,6 +6,8 @@ parity_util: indices exact up to near ties (counted), weights 1e-5 absolute,
 integer and byte outputs bit-exact given the same indices, combine 1e-2
 relative.  Nothing flows from the GPU into the oracle.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -753,3 +755,26 @@ def test_random_shapes_whole_path_match_oracle(N, H, E, K, skew, renorm):
     _, _, r, _ = oracle.dispatch(idx.cpu().numpy(), E)
     ref = oracle.combine(bits(Y), r, tw.cpu().numpy())
     combine_close(bits(out), ref)
+
+
+def test_route_dispatch_noncooperative_launch_in_a_child_process():
+    # MOE_FUSED_LAUNCH=noncooperative (read once per process): the same one launch without the
+    # cooperative attribute gives the same results
+    import subprocess
+    import sys
+    code = (
+        "import numpy as np, torch, combine_moe_route_02_gb300 as moe, moe_inputs as mi, oracle\n"
+        "moe.lib()\n"
+        "X, W, _ = mi.make_route_inputs(2048, 1024, 64, 11)\n"
+        "st = torch.zeros(1, dtype=torch.int32, device='cuda')\n"
+        "idx, tw, d, n = moe.route_dispatch(X.cuda(), W.cuda(), 2, status=st)\n"
+        "torch.cuda.synchronize()\n"
+        "assert st.item() == 0 and n == 1, (st.item(), n)\n"
+        "c, o, r, s = oracle.dispatch(idx.cpu().numpy(), 64)\n"
+        "assert np.array_equal(d.row_map.cpu().numpy(), r)\n"
+        "assert np.array_equal(mi.bf16_bits(d.X_perm.cpu()), oracle.permute(mi.bf16_bits(X), r, 2))\n"
+        "print('ok')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MOE_FUSED_LAUNCH="noncooperative", PYTHONPATH=root)
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0 and out.stdout.strip().endswith("ok"), out.stderr[-2000:]
