@@ -269,6 +269,24 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
 
     const int chunks = p.H >> 3;
     const bool pf = p.d_prefetch && p.d_Xp != nullptr && ntok > 0;
+    // this warp's slot ids (slot i = token i / K, rank i % K), as the epilogue
+    // left them in the selection window, in registers before the row prefetch
+    // may overwrite that memory; ids outside [0, E) become E (skipped)
+    constexpr int kIdIters = ((kBM / 2 * KMAX + kWarps - 1) / kWarps + 31) / 32;   // R <= kBM / 2
+    int ids[kIdIters];
+    {
+        const int *ids_s = reinterpret_cast<const int *>(smem + p.win_off) + R;
+#pragma unroll
+        for (int j = 0; j < kIdIters; ++j) {
+            const int i = w0 + lane + 32 * j;
+            int e = E;
+            if (i < w1) {
+                const int t = i / K;
+                e = ids_s[(i - t * K) * kBM + t];
+            }
+            ids[j] = (e < 0 || e >= E) ? E : e;
+        }
+    }
     // the rows this CTA will copy do not depend on the dispatch: start their
     // bulk copy into shared memory now (the router is done with all of it)
     fence_proxy_async_smem();
@@ -285,15 +303,15 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
         before[e] = 0;
     }
     __syncthreads();
-    // per-warp histograms of contiguous slot ranges (ids written by this CTA
-    // before the last block-wide barrier)
-    for (int base = w0; base < w1; base += 32) {
-        const int i = base + lane;
-        int e = i < w1 ? p.topk_idx[s0 + i] : E;
-        if (e < 0 || e >= E) e = E;
-        const uint32_t peers = same_key_lanes(e);
-        if (e < E && lane == __ffs(peers) - 1) my_cnt[e] += __popc(peers);
-        __syncwarp();
+    // per-warp histograms of contiguous slot ranges
+#pragma unroll
+    for (int j = 0; j < kIdIters; ++j) {
+        if (w0 + 32 * j < w1) {   // warp-uniform
+            const int e = ids[j];
+            const uint32_t peers = same_key_lanes(e);
+            if (e < E && lane == __ffs(peers) - 1) my_cnt[e] += __popc(peers);
+            __syncwarp();
+        }
     }
     __syncthreads();
     for (int e = tid; e < E; e += kThreads) {
@@ -396,21 +414,23 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
     __syncthreads();
 
     // stable scatter: slot i of this CTA gets row offset + before + its rank
-    for (int base = w0; base < w1; base += 32) {
-        const int i = base + lane;
-        int e = i < w1 ? p.topk_idx[s0 + i] : E;
-        if (e < 0 || e >= E) e = E;
-        const uint32_t peers = same_key_lanes(e);
-        const uint32_t below = peers & ((1u << lane) - 1u);
-        if (i < w1) {
-            const int r = e < E ? my_cnt[e] + __popc(below) : -1;
-            rows_s[i] = r;
-            p.d_row_map[s0 + i] = r;
-            if (e < E && p.d_src_slot) p.d_src_slot[r] = static_cast<int32_t>(s0 + i);
+#pragma unroll
+    for (int j = 0; j < kIdIters; ++j) {
+        if (w0 + 32 * j < w1) {   // warp-uniform
+            const int i = w0 + 32 * j + lane;
+            const int e = ids[j];
+            const uint32_t peers = same_key_lanes(e);
+            const uint32_t below = peers & ((1u << lane) - 1u);
+            if (i < w1) {
+                const int r = e < E ? my_cnt[e] + __popc(below) : -1;
+                rows_s[i] = r;
+                p.d_row_map[s0 + i] = r;
+                if (e < E && p.d_src_slot) p.d_src_slot[r] = static_cast<int32_t>(s0 + i);
+            }
+            __syncwarp();
+            if (e < E && below == 0) my_cnt[e] += __popc(peers);
+            __syncwarp();
         }
-        __syncwarp();
-        if (e < E && below == 0) my_cnt[e] += __popc(peers);
-        __syncwarp();
     }
 
     // the last CTA to leave returns the barrier counters to zero
@@ -470,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                                                                const __grid_constant__ CUtensorMap tmW,
                                                                const TcParams p)
 {
+    static_assert(SPLIT || !FUSE, "the dispatch tail takes its ids from the split-mode epilogue");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms, as an offset from the
     // shared array: a pointer derived this way keeps its shared address space,
@@ -875,6 +896,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                 topk_pop_if<KMAX>(bk, bi, bi[0] == i);
                 if (part == 0) {
                     wrow[k * kBM] = fv;
+                    // the dispatch tail's copy of the id: window rows R .. 2R - 1 are unused (S >= 2)
+                    if constexpr (FUSE) reinterpret_cast<int *>(wrow)[k * kBM + R] = i;
                     if (n < p.N) {
                         p.topk_idx[static_cast<int64_t>(n) * K + k] = i;
                         if (p.counts && i < E) atomicAdd(hist_s + i, 1);
