@@ -144,11 +144,37 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _status_ptr(status: Optional[torch.Tensor]):
+    """The device status word (one int32 on the current device), or None."""
+    if status is None:
+        return None
+    _need(status, "status", torch.int32)
+    if status.numel() < 1:
+        raise ValueError("status must hold at least one int32")
+    return _status_ptr(status)
+
+
+def _workspace_arg(ws: Optional[torch.Tensor]):
+    """(pointer, size in bytes) of a workspace tensor of any dtype, or (None, 0)."""
+    if ws is None:
+        return None, 0
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if ws.device.index != torch.cuda.current_device():
+        raise ValueError(f"workspace is on {ws.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}")
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
 def _need(t: torch.Tensor, name: str, dtype, shape=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device and takes raw pointers
+        raise ValueError(f"{name} is on {t.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()} (select it with torch.cuda.device)")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -175,7 +201,7 @@ def route(X: torch.Tensor, W_gate: torch.Tensor, K: int, bias: Optional[torch.Te
     _need(topk_idx, "topk_idx", torch.int32, (N, K))
     _need(topk_w, "topk_w", torch.float32, (N, K))
     code = lib().moe_route_ex(_ptr(X), _ptr(W_gate), _ptr(bias), N, H, E, K, int(bool(renorm)),
-                              _ptr(topk_idx), _ptr(topk_w), _ptr(status), _ALGOS[algo], _stream(stream))
+                              _ptr(topk_idx), _ptr(topk_w), _status_ptr(status), _ALGOS[algo], _stream(stream))
     _check(code, "moe_route")
     return topk_idx, topk_w
 
@@ -197,7 +223,7 @@ def route_stats(X: torch.Tensor, W_gate: torch.Tensor, K: int, bias: Optional[to
     lse = torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None
     counts = torch.empty(E, dtype=torch.int32, device=dev) if want_counts else None
     code = lib().moe_route_stats(_ptr(X), _ptr(W_gate), _ptr(bias), N, H, E, K, int(bool(renorm)),
-                                 _ptr(topk_idx), _ptr(topk_w), _ptr(lse), _ptr(counts), _ptr(status),
+                                 _ptr(topk_idx), _ptr(topk_w), _ptr(lse), _ptr(counts), _status_ptr(status),
                                  _ALGOS[algo], _stream(stream))
     _check(code, "moe_route_stats")
     return topk_idx, topk_w, lse, counts
@@ -251,7 +277,10 @@ def dispatch_workspace(E: int, device=None, stream=None) -> torch.Tensor:
     key = (device.index, stream.cuda_stream, E)
     ws = _workspaces.get(key)
     if ws is None:
-        ws = torch.zeros(dispatch_workspace_size(0, E, 1), dtype=torch.uint8, device=device)
+        # zero-filled on the stream that will use it, so the first call there is
+        # ordered after the fill
+        with torch.cuda.stream(stream):
+            ws = torch.zeros(dispatch_workspace_size(0, E, 1), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 
@@ -298,7 +327,7 @@ def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, f
         _ptr(topk_idx), _ptr(X), N, H, E, K, _ptr(out.expert_counts), _ptr(out.expert_offsets),
         _ptr(out.row_map), _ptr(out.src_slot), _ptr(out.X_perm) if has_x else None,
         _ptr(out.X_fp8) if has_x else None, _ptr(out.X_scale) if has_x else None, fmt,
-        _ptr(status), _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
+        _status_ptr(status), *_workspace_arg(workspace), _stream(stream))
     _check(code, "moe_dispatch_ex")
     return out
 
@@ -337,7 +366,7 @@ def route_dispatch(X: torch.Tensor, W_gate: torch.Tensor, K: int, bias: Optional
     code = lib().moe_route_dispatch(
         _ptr(X), _ptr(W_gate), _ptr(bias), N, H, E, K, int(bool(renorm)), _ptr(topk_idx), _ptr(topk_w),
         _ptr(out.expert_counts), _ptr(out.expert_offsets), _ptr(out.row_map), _ptr(out.src_slot),
-        _ptr(out.X_perm), _ptr(status), _ptr(workspace), workspace.numel(), ctypes.byref(launches),
+        _ptr(out.X_perm), _status_ptr(status), *_workspace_arg(workspace), ctypes.byref(launches),
         _stream(stream))
     _check(code, "moe_route_dispatch")
     return topk_idx, topk_w, out, launches.value
@@ -387,8 +416,8 @@ def dispatch_ep(topk_idx: torch.Tensor, E: int, ep_size: int, X: Optional[torch.
     code = lib().moe_dispatch_ep(
         _ptr(topk_idx), _ptr(X), N, H, E, K, ep_size, _ptr(out.expert_counts), _ptr(out.expert_offsets),
         _ptr(out.row_map), _ptr(out.rank_counts), _ptr(out.rank_offsets), _ptr(out.send_token),
-        _ptr(out.slot_send_row), _ptr(out.expand_idx), _ptr(out.send_meta), _ptr(out.X_send), _ptr(status),
-        _ptr(workspace), workspace.numel(), _stream(stream))
+        _ptr(out.slot_send_row), _ptr(out.expand_idx), _ptr(out.send_meta), _ptr(out.X_send), _status_ptr(status),
+        *_workspace_arg(workspace), _stream(stream))
     _check(code, "moe_dispatch_ep")
     return out
 
@@ -408,7 +437,7 @@ def permute(X: torch.Tensor, row_map: torch.Tensor, K: int, bf16: bool = True, f
         X_fp8 = torch.empty((N * K, H), dtype=torch.uint8, device=dev)
         X_scale = torch.empty((N * K, H // 128), dtype=_scale_dtype(scale_format), device=dev)
     code = lib().moe_permute_ex(_ptr(X), _ptr(row_map), N, H, K, _ptr(X_perm), _ptr(X_fp8), _ptr(X_scale), fmt,
-                                _ptr(status), _stream(stream))
+                                _status_ptr(status), _stream(stream))
     _check(code, "moe_permute_ex")
     return X_perm, X_fp8, X_scale
 
@@ -427,12 +456,12 @@ def combine(Y: torch.Tensor, row_map: torch.Tensor, topk_w: torch.Tensor, out=No
         out = torch.empty((N, H), dtype=torch.bfloat16, device=Y.device)
     _need(out, "out", torch.bfloat16, (N, H))
     if residual is None:
-        code = lib().moe_combine(_ptr(Y), _ptr(row_map), _ptr(topk_w), N, H, K, _ptr(out), _ptr(status),
+        code = lib().moe_combine(_ptr(Y), _ptr(row_map), _ptr(topk_w), N, H, K, _ptr(out), _status_ptr(status),
                                  _stream(stream))
         _check(code, "moe_combine")
     else:
         _need(residual, "residual", torch.bfloat16, (N, H))
         code = lib().moe_combine_residual(_ptr(Y), _ptr(row_map), _ptr(topk_w), _ptr(residual), N, H, K,
-                                          _ptr(out), _ptr(status), _stream(stream))
+                                          _ptr(out), _status_ptr(status), _stream(stream))
         _check(code, "moe_combine_residual")
     return out

@@ -56,7 +56,9 @@ constexpr int kBK = 64;                        // bf16 per 128-byte swizzle row 
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // 320
 constexpr int kWarps = kThreads / 32;
-constexpr int kFuseMaxCtas = 1024;   // rows of the per-CTA count table in the dispatch workspace
+// rows of the per-CTA count table in the dispatch workspace: the same bound as the
+// dispatch kernel's table (dispatch.cu), which sizes moe_dispatch_workspace_size()
+constexpr int kFuseMaxCtas = 1024;
 constexpr int64_t kFuseMaxCopyBytes = 32ll << 20;   // fused row copies up to this size
 constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KiB X tile per slot
 constexpr uint32_t kBBoxBytes = kBK * 64 * 2;  // 8 KiB per 64-expert gate box

@@ -189,6 +189,18 @@ def test_binding_refuses_cpu_tensors():
         moe.route(X, W, 2)
 
 
+def test_binding_checks_status_word_and_workspace():
+    # the status word and the workspace reach the kernels as raw pointers: a host
+    # tensor is refused before the library is called, and a workspace's size is
+    # its byte count whatever its dtype
+    assert moe._status_ptr(None) is None
+    with pytest.raises(ValueError, match="CUDA"):
+        moe._status_ptr(torch.zeros(1, dtype=torch.int32))
+    assert moe._workspace_arg(None) == (None, 0)
+    with pytest.raises(ValueError, match="CUDA"):
+        moe._workspace_arg(torch.zeros(64, dtype=torch.int32))
+
+
 def test_product_does_not_import_oracle():
     # the product path (package + CUDA sources) never imports, links or loads the oracle
     here = os.path.dirname(moe.__file__)

@@ -389,6 +389,26 @@ def test_dispatch_workspace_reused_many_times():
     assert int(ws[:8].abs().sum()) == 0
 
 
+def test_dispatch_on_a_side_stream_with_an_int32_workspace():
+    # the binding passes a workspace's size in bytes whatever its dtype, and the
+    # cached workspace of a new (stream, E) is zeroed on that stream
+    side = torch.cuda.Stream()
+    N, E, K = 3000, 40, 3
+    idx = mi.random_topk_idx(N, E, K, seed=11)
+    c, o, r, s = oracle.dispatch(idx.numpy(), E)
+    ws32 = torch.zeros(moe.dispatch_workspace_size(0, E, 1) // 4, dtype=torch.int32, device=DEV)
+    idx_d = idx.to(DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        d1 = moe.dispatch(idx_d, E, workspace=ws32, stream=side)
+        d2 = moe.dispatch(idx_d, E, stream=side)
+    torch.cuda.synchronize()
+    for d in (d1, d2):
+        assert np.array_equal(d.expert_counts.cpu().numpy(), c)
+        assert np.array_equal(d.row_map.cpu().numpy(), r)
+    assert int(ws32[:2].abs().sum()) == 0
+
+
 @pytest.mark.parametrize("N,H,K", [(1, 128, 1), (100, 128, 8), (257, 384, 2), (64, 4096, 4), (300, 2048, 8),
                                    (7, 256, 16)])
 def test_permute_ue8m0_scales_match_oracle(N, H, K):
