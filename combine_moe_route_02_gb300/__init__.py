@@ -151,7 +151,7 @@ def _status_ptr(status: Optional[torch.Tensor]):
     _need(status, "status", torch.int32)
     if status.numel() < 1:
         raise ValueError("status must hold at least one int32")
-    return _status_ptr(status)
+    return _ptr(status)
 
 
 def _workspace_arg(ws: Optional[torch.Tensor]):

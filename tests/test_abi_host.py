@@ -201,6 +201,16 @@ def test_binding_checks_status_word_and_workspace():
         moe._workspace_arg(torch.zeros(64, dtype=torch.int32))
 
 
+def test_binding_status_word_pointer(monkeypatch):
+    # with the device checks stubbed out (no GPU here), an accepted status word
+    # is passed as its own data pointer
+    monkeypatch.setattr(moe, "_need", lambda t, name, dtype, shape=None: t)
+    st = torch.zeros(1, dtype=torch.int32)
+    assert moe._status_ptr(st).value == st.data_ptr()
+    with pytest.raises(ValueError, match="at least one"):
+        moe._status_ptr(torch.zeros(0, dtype=torch.int32))
+
+
 def test_product_does_not_import_oracle():
     # the product path (package + CUDA sources) never imports, links or loads the oracle
     here = os.path.dirname(moe.__file__)
