@@ -7,6 +7,7 @@ no torch extension machinery: the library has a plain C ABI.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -53,11 +54,27 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
+def _fresh() -> bool:
+    return os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _deps_mtime()
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile (if stale) and return the path of the shared library."""
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _deps_mtime():
+    """Compile (if stale) and return the path of the shared library.
+
+    Concurrent builds (several processes importing the package at once) are
+    serialised by an exclusive lock on a file in the build folder: they share
+    its object files, and a process that waited finds the library fresh."""
+    if not force and _fresh():
         return LIB_PATH
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and _fresh():
+            return LIB_PATH
+        return _build_locked(verbose_ptxas)
+
+
+def _build_locked(verbose_ptxas: bool) -> str:
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
