@@ -688,6 +688,54 @@ def test_route_dispatch_workspace_reused():
         assert np.array_equal(bits(d.X_perm), oracle.permute(bits(X), r, K))
 
 
+def test_concurrent_host_threads_on_their_own_streams():
+    # the library is reentrant: its host state (plan caches, function attributes)
+    # is shared by threads calling it at once, each on its own stream with its
+    # own workspace; the kernels are deterministic, so every concurrent result
+    # equals the same call made alone
+    import threading
+    shapes = [(512, 256, 16, 2), (2048, 1024, 64, 2), (4096, 2048, 64, 4), (777, 512, 32, 3)]
+    inputs, alone = [], []
+    for t, (N, H, E, K) in enumerate(shapes):
+        X, W, _ = mi.make_route_inputs(N, H, E, seed=100 + t)
+        Xd, Wd = X.to(DEV), W.to(DEV)
+        idx, tw, d, n = moe.route_dispatch(Xd, Wd, K)
+        out = moe.combine(d.X_perm, d.row_map, tw)
+        torch.cuda.synchronize()
+        inputs.append((Xd, Wd, K, E))
+        alone.append((idx.cpu(), tw.cpu(), d.row_map.cpu(), d.X_perm.cpu(), out.cpu()))
+    errors = []
+
+    def worker(t):
+        try:
+            Xd, Wd, K, E = inputs[t]
+            stream = torch.cuda.Stream()
+            ws = torch.zeros(moe.dispatch_workspace_size(0, E, 1), dtype=torch.uint8, device=DEV)
+            st = status_word()
+            stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(stream):
+                for _ in range(10):
+                    idx, tw, d, n = moe.route_dispatch(Xd, Wd, K, workspace=ws, status=st, stream=stream)
+                    out = moe.combine(d.X_perm, d.row_map, tw, status=st, stream=stream)
+                    stream.synchronize()
+                    got = (idx.cpu(), tw.cpu(), d.row_map.cpu(), d.X_perm.cpu(), out.cpu())
+                    for a, b in zip(got, alone[t]):
+                        if not torch.equal(a, b):
+                            errors.append(f"shape {shapes[t]}: differs from the call made alone")
+                            return
+            if st.item() != 0:
+                errors.append(f"shape {shapes[t]}: {moe.status_string(st.item())}")
+        except Exception as exc:  # reported in the main thread
+            errors.append(f"shape {shapes[t]}: {exc!r}")
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(len(shapes))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+
+
 def test_route_dispatch_empty():
     N, H, E, K = 0, 256, 16, 2
     X = torch.empty((0, H), dtype=torch.bfloat16, device=DEV)
