@@ -73,6 +73,37 @@ def test_gpu_line_has_the_contract_keys():
     assert d["roofline"]["kernel"] in ("route_dispatch", "combine")
 
 
+GPU_VARIANTS = {
+    "apart": (["--apart"], lambda c: c["calls"] == "moe_route, moe_dispatch, moe_combine"),
+    "residual": (["--residual"], lambda c: "residual" in c["combine"]),
+    "route_stats": (["--route-stats"], lambda c: "moe_route_stats" in c["route"]),
+    "ue8m0": (["--workload", "moe_layer_n16384_h2048_e128_k8_fp8", "--scale-format", "ue8m0"],
+              lambda c: c["fp8_scales"] == "ue8m0"),
+    "ep": (["--workload", "n4096_h2048_e64_k4", "--ep-size", "4"], lambda c: "ep_size 4" in c["dispatch"]),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("variant", sorted(GPU_VARIANTS))
+def test_gpu_variant_lines(variant):
+    # every bench variant still runs end to end and names itself in its config
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    extra, names_itself = GPU_VARIANTS[variant]
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "5", "--warmup", "3", "--no-cpu-baseline",
+           "--e2e-steps", "8", "--no-torch-naive", *extra]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert names_itself(d["config"]), d["config"]
+    assert d["value"] > 0 and d["e2e"]["value"] > 0 and d["gpu_launches"] >= 2 * d["steps"]
+    r = d["roofline"]
+    assert r["peak"] > 0 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+
+
 def test_source_digest_ignores_comments_only():
     import bench
     a = 'int f(int x) { // add one\n  return x + 1; /* done */ }\nconst char *s = "// kept";\n'
