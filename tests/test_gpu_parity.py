@@ -736,6 +736,32 @@ def test_concurrent_host_threads_on_their_own_streams():
     assert not errors, errors
 
 
+def test_route_dispatch_repeatable_back_to_back():
+    # the one-launch route + dispatch is deterministic: thousands of back-to-back
+    # calls (two shapes alternating on one workspace, no host sync in between)
+    # give bit-identical ids, weights, maps and rows every time; a race in the
+    # grid barrier or the split-K exchange would show up as a mismatch
+    cases = []
+    for t, (N, H, E, K) in enumerate([(2048, 1024, 64, 2), (512, 256, 16, 2)]):
+        X, W, _ = mi.make_route_inputs(N, H, E, seed=200 + t)
+        Xd, Wd = X.to(DEV), W.to(DEV)
+        idx, tw, d, n = moe.route_dispatch(Xd, Wd, K)
+        assert n == 1
+        cases.append((Xd, Wd, K, E, idx.clone(), tw.clone(), d.row_map.clone(), d.X_perm.clone()))
+    E_max = max(c[3] for c in cases)
+    ws = torch.zeros(moe.dispatch_workspace_size(0, E_max, 1), dtype=torch.uint8, device=DEV)
+    st = status_word()
+    bad = torch.zeros((), dtype=torch.int64, device=DEV)
+    for i in range(4000):
+        Xd, Wd, K, E, ri, rw, rm, rp = cases[i % 2]
+        idx, tw, d, n = moe.route_dispatch(Xd, Wd, K, workspace=ws, status=st)
+        bad += (idx != ri).any() | (tw != rw).any() | (d.row_map != rm).any() | (d.X_perm != rp).any()
+    torch.cuda.synchronize()
+    assert st.item() == 0, moe.status_string(st.item())
+    assert int(bad) == 0
+    assert int(ws[:8].view(torch.int32).abs().sum()) == 0
+
+
 def test_route_dispatch_empty():
     N, H, E, K = 0, 256, 16, 2
     X = torch.empty((0, H), dtype=torch.bfloat16, device=DEV)
