@@ -7,7 +7,9 @@
  *  - All tensor arguments are DEVICE pointers to row-major, contiguous
  *    buffers that the caller owns.  The library allocates and frees nothing,
  *    keeps no per-call state between calls and may be called from several
- *    host threads at once (each call only touches its own arguments).
+ *    host threads at once (each call only touches its own arguments).  Calls
+ *    that may run at the same time on the GPU (other streams, other threads)
+ *    must not share a dispatch workspace: it holds grid-barrier counters.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream) and never synchronises the host, so a sequence
  *    of calls can be captured into a CUDA graph.
