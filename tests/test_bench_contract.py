@@ -46,6 +46,25 @@ def test_reference_line_names_the_variant():
     assert "moe_route_stats" in d["config"]["route"]
 
 
+def test_reference_arm_under_torchrun_prints_one_line():
+    # the launch used for N > 1: rank 0 alone runs the reference arm and prints
+    # its line, the other rank exits 0 without work (no GPU, no process group)
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1",
+           "--workload", "tiny_n512_h256_e16_k2"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
 @pytest.mark.gpu
 def test_gpu_line_has_the_contract_keys():
     import torch
