@@ -8,7 +8,12 @@
  *   - every permuted row is the bit pattern of its token's row of X;
  *   - with the expert outputs Y = X_perm, the combine gives sum_k w_k * X[n] = X[n] (to bf16
  *     rounding), because the weights sum to 1;
- *   - moe_route_dispatch gives the same ids, weights and dispatch as the two calls.
+ *   - moe_route_dispatch gives the same ids, weights and dispatch as the two calls;
+ *   - moe_combine_residual with residual = X gives 2 X (to bf16 rounding);
+ *   - moe_route_stats gives the same ids and weights, the dispatch's expert counts,
+ *     and each token's logsumexp (checked against one taken here in fp64);
+ *   - moe_load_stats gives the mean, max/mean, P95/mean and z-loss of those
+ *     counts and logsumexps as defined.
  * Prints "ok" and returns 0, or prints the first failure and returns 1.
  */
 #include <math.h>
@@ -185,6 +190,76 @@ int main(void)
     if (memcmp(hc, hc2, 4 * E) != 0 || memcmp(ho, ho2, 4 * (E + 1)) != 0 || memcmp(hr, hr2, 4 * S) != 0 ||
         memcmp(hs, hs2, 4 * S) != 0 || memcmp(hp, hp2, sizeof(uint16_t) * S * H) != 0)
         return fail("moe_route_dispatch dispatches differently");
+
+    /* combine with the residual connection, residual = X: out = X + X */
+    void *out2;
+    CUDA_OK(cudaMalloc(&out2, sizeof(uint16_t) * N * H));
+    MOE_OK_(moe_combine_residual(Xp, rmap, w, X, N, H, K, out2, status, ms));
+    /* router statistics (renorm on), then the load statistics of its counts */
+    int32_t *idx3, *cnt3;
+    float *w3, *lse, *stats;
+    CUDA_OK(cudaMalloc((void **)&idx3, 4 * S));
+    CUDA_OK(cudaMalloc((void **)&w3, 4 * S));
+    CUDA_OK(cudaMalloc((void **)&cnt3, 4 * E));
+    CUDA_OK(cudaMalloc((void **)&lse, 4 * N));
+    CUDA_OK(cudaMalloc((void **)&stats, 4 * 4));
+    const float z_coef = 1e-3f;
+    MOE_OK_(moe_route_stats(X, W, NULL, N, H, E, K, 1, idx3, w3, lse, cnt3, status, MOE_ROUTE_AUTO, ms));
+    MOE_OK_(moe_load_stats(cnt3, E, lse, N, z_coef, stats, ms));
+    CUDA_OK(cudaStreamSynchronize(s));
+    CUDA_OK(cudaMemcpy(&st, status, 4, cudaMemcpyDeviceToHost));
+    if (st != 0) return fail(moe_status_string((moe_status)st));
+
+    uint16_t *hout2 = malloc(sizeof(uint16_t) * N * H);
+    int32_t *hi3 = malloc(4 * S), *hc3 = malloc(4 * E);
+    float *hw3 = malloc(4 * S), *hl = malloc(4 * N), hst[4];
+    CUDA_OK(cudaMemcpy(hout2, out2, sizeof(uint16_t) * N * H, cudaMemcpyDeviceToHost));
+    CUDA_OK(cudaMemcpy(hi3, idx3, 4 * S, cudaMemcpyDeviceToHost));
+    CUDA_OK(cudaMemcpy(hw3, w3, 4 * S, cudaMemcpyDeviceToHost));
+    CUDA_OK(cudaMemcpy(hc3, cnt3, 4 * E, cudaMemcpyDeviceToHost));
+    CUDA_OK(cudaMemcpy(hl, lse, 4 * N, cudaMemcpyDeviceToHost));
+    CUDA_OK(cudaMemcpy(hst, stats, sizeof(hst), cudaMemcpyDeviceToHost));
+
+    for (int64_t i = 0; i < N * H; ++i) {
+        const float x2 = 2.0f * from_bf16(hX[i]), o = from_bf16(hout2[i]);
+        if (fabsf(o - x2) > 1e-2f * fabsf(x2) + 1e-6f) return fail("combine with residual differs from 2 X");
+    }
+    if (memcmp(hi, hi3, 4 * S) != 0 || memcmp(hw, hw3, 4 * S) != 0) return fail("moe_route_stats routes differently");
+    if (memcmp(hc, hc3, 4 * E) != 0) return fail("router histogram differs from the dispatch counts");
+    /* logsumexp of the logits, taken here in fp64 from the same bf16 operands */
+    for (int64_t n = 0; n < N; ++n) {
+        double L[NEXP], m = -INFINITY, z = 0.0;
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h) acc += (double)from_bf16(hX[n * H + h]) * (double)from_bf16(hW[h * E + e]);
+            L[e] = acc;
+            if (acc > m) m = acc;
+        }
+        for (int e = 0; e < E; ++e) z += exp(L[e] - m);
+        const double ref = m + log(z);
+        if (fabs((double)hl[n] - ref) > 1e-3 + 1e-5 * fabs(ref)) return fail("logsumexp differs from fp64");
+    }
+    /* load statistics: the mean, max/mean, P95/mean (linear interpolation) and z-loss */
+    double mean = (double)S / E, cmax = 0.0, zsum = 0.0;
+    int32_t sorted[NEXP];
+    memcpy(sorted, hc3, sizeof(sorted));
+    for (int i = 1; i < E; ++i)   /* insertion sort of E counts */
+        for (int j = i; j > 0 && sorted[j - 1] > sorted[j]; --j) {
+            const int32_t t = sorted[j];
+            sorted[j] = sorted[j - 1];
+            sorted[j - 1] = t;
+        }
+    cmax = sorted[E - 1];
+    const double pos = 0.95 * (E - 1);
+    const int lo = (int)pos;
+    const double p95 = sorted[lo] + (pos - lo) * ((lo + 1 < E ? sorted[lo + 1] : sorted[lo]) - sorted[lo]);
+    for (int64_t n = 0; n < N; ++n) zsum += (double)hl[n] * (double)hl[n];
+    const double zloss = (double)z_coef * zsum / (double)N;
+    if (fabs(hst[3] - mean) > 1e-6 * mean) return fail("load stats: mean");
+    if (fabs(hst[0] - cmax / mean) > 1e-6 * (cmax / mean)) return fail("load stats: max / mean");
+    if (fabs(hst[1] - p95 / mean) > 1e-6 * (p95 / mean)) return fail("load stats: P95 / mean");
+    if (fabs(hst[2] - zloss) > 1e-5 * zloss + 1e-9) return fail("load stats: z-loss");
+
     printf("ok (moe_route_dispatch: %d launch%s)\n", launches, launches == 1 ? "" : "es");
     return 0;
 }
