@@ -2,8 +2,9 @@
 """Benchmark of the MoE routing hot path on GB300: route -> dispatch -> permute -> combine.
 
 One step = one pass of the whole path over one batch of synthetic tokens
-(default workload n2048_h1024_e64_k2: N=2048, H=1024, E=64, K=2), inputs
-resident in HBM.  Prints ONE JSON line (rank 0).
+(default workload skewed_zipf_n65536_h4096_e64_k2: N=65536, H=4096, E=64, K=2
+with a Zipf-like per-expert logit bias -- the largest of the five workloads),
+inputs resident in HBM.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -12,10 +13,13 @@ a 256 MiB buffer is written to flush the 129 MB L2; each step is bracketed by
 CUDA events on the launching stream (the flush is outside the brackets), and
 every kernel of the step has its own event pair.  Under torchrun each rank
 runs its own replica on its own token batch (weak scaling, no collective on
-the data path); the reported time is the max over ranks.
+the data path); the reported time is the max over ranks.  Every rank shares one gate weight
+(the replica layout: tokens differ per rank, W_gate does not).
 
 --impl reference times the CPU oracle (oracle/, fp64 C) on the same workload on
 this machine's host cores: the only other implementation of this path here.
+Each of its steps is a bounded sample of the workload (its first T tokens, T
+sized so that the whole run takes about REF_BUDGET_S seconds).
 """
 from __future__ import annotations
 
@@ -44,6 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 E2E_UNIT = 64          # pipelined end-to-end steps per CUDA graph
 E2E_BUFFERS = 2        # buffer sets of the pipelined end-to-end steps (3 or 4 measured no faster)
 L2_FLUSH_BYTES = 256 << 20
+REF_BUDGET_S = 120.0   # wall time of the reference arm's warm-up + timed steps
 
 
 def parse_args():
@@ -82,7 +87,9 @@ def dist_env():
 
 KERNEL_SOURCES = {"route": "route_tc.cu", "dispatch": "dispatch.cu", "combine": "combine.cu",
                   "route_dispatch": "route_tc.cu"}
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+# ncu DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum), one row
+# per (kernel, workload), with a digest of the kernel's source at capture time
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.csv")
 
 
 def code_only(text: str) -> str:
@@ -116,23 +123,23 @@ def source_digest(kernel: str) -> str:
         return hashlib.sha256(code_only(f.read()).encode()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch (read + write) from the committed ncu summary, or
-    None when there is none for this kernel/workload or the kernel's source has
-    changed since it was taken (the summary records a digest of the source)."""
+def ncu_traffic(kernel: str, workload: str, path: str = None):
+    """DRAM bytes per launch (read + write) from the ncu capture table, or None when
+    there is no row for this kernel/workload or the kernel's source has changed since
+    the capture (each row records a digest of the source)."""
+    import csv
     try:
-        with open(TRAFFIC_FILE) as f:
-            lines = f.read().splitlines()
+        with open(path or TRAFFIC_FILE, newline="") as f:
+            rows = list(csv.DictReader(f))
     except OSError:
         return None
-    for line in lines:
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload:
+    for r in rows:
+        if r.get("kernel") == kernel and r.get("workload") == workload:
             try:
-                value = float(cells[2])
-            except ValueError:
+                value = float(r["dram_bytes_per_launch"])
+            except (KeyError, TypeError, ValueError):
                 continue
-            return value if cells[3] == source_digest(kernel) else None
+            return value if r.get("source_digest") == source_digest(kernel) else None
     return None
 
 
@@ -292,37 +299,66 @@ def residual_rows(w: mi.Workload, rank: int = 0):
     return mi.random_bf16((w.N, w.H), seed=1000 + rank)
 
 
+def oracle_sample(w: mi.Workload, T: int, X=None, W=None, bias=None):
+    """The first T tokens of the workload as the oracle takes them: (Xb, Wb, bias,
+    Y), with the expert outputs Y of that sample built by the oracle (untimed)."""
+    import oracle
+    if X is None:
+        X, W, bias = mi.make_workload_inputs(w)
+    Xb, Wb = mi.bf16_bits(X[:T]), mi.bf16_bits(W)
+    b = None if bias is None else bias.numpy()
+    Y = oracle.run_path(Xb, Wb, b, w.K, w.renorm, w.fp8)["Y"]
+    return Xb, Wb, b, Y
+
+
+def oracle_seconds_per_token(w: mi.Workload, Xb, Wb, b, Y, probe_tokens: int, **kw) -> float:
+    """Host seconds per token of one oracle pass, measured on the first probe_tokens tokens."""
+    import oracle
+    T = min(probe_tokens, Xb.shape[0])
+    sw = mi.Workload(w.name, T, w.H, w.E, w.K, w.renorm, w.fp8, w.skew)
+    Ys = Y if T == Xb.shape[0] else oracle.run_path(Xb[:T], Wb, b, w.K, w.renorm, w.fp8)["Y"]
+    t0 = time.perf_counter()
+    oracle_pass(oracle, Xb[:T], Wb, b, sw, Ys, **kw)
+    return (time.perf_counter() - t0) / T
+
+
 def cpu_baseline(w: mi.Workload, seconds: float, max_reps: int = 1000, residual: bool = False,
                  ue8m0: bool = False, ep_size: int = 0, stats: bool = False):
+    """The oracle on the host cores over a bounded sample of the workload: passes over
+    its first T tokens (T sized for about one second per pass) for `seconds`, then on
+    one host thread over a smaller sample for about seconds / 2."""
     import oracle
     X, W, bias = mi.make_workload_inputs(w)
-    Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
-    b = None if bias is None else bias.numpy()
-    r = oracle.run_path(Xb, Wb, b, w.K, w.renorm, w.fp8)   # untimed: provides the expert outputs Y
-    Y = r["Y"]
-    R = mi.bf16_bits(residual_rows(w)) if residual else None
-    def timed(limit_s):
+    kw = dict(ue8m0=ue8m0, ep_size=ep_size, stats=stats)
+    cores = oracle.num_threads()
+
+    def run(threads, per_pass_s, limit_s):
+        oracle.set_num_threads(threads)
+        probe = mi.Workload(w.name, min(w.N, 1024), w.H, w.E, w.K, w.renorm, w.fp8, w.skew)
+        pXb, pWb, pb, pY = oracle_sample(probe, probe.N, X, W, bias)
+        spt = oracle_seconds_per_token(w, pXb, pWb, pb, pY, probe.N, **kw)
+        T = int(max(64, min(w.N, per_pass_s / max(spt, 1e-12))))
+        sw = mi.Workload(w.name, T, w.H, w.E, w.K, w.renorm, w.fp8, w.skew)
+        Xb, Wb, b, Y = oracle_sample(sw, T, X, W, bias)
+        R = mi.bf16_bits(residual_rows(w)[:T]) if residual else None
         reps, t0 = 0, time.perf_counter()
         while True:
-            oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, ep_size, stats)
+            oracle_pass(oracle, Xb, Wb, b, sw, Y, R, **kw)
             reps += 1
             el = time.perf_counter() - t0
             if el >= limit_s or reps >= max_reps:
-                return reps, el
+                return T, reps, el
 
-    cores = oracle.num_threads()
-    reps, el = timed(seconds)
-    # the same on one host thread, for a bounded sample (about half as long)
-    oracle.set_num_threads(1)
     try:
-        reps1, el1 = timed(seconds / 2)
+        T, reps, el = run(cores, min(1.0, seconds / 5), seconds)
+        T1, reps1, el1 = run(1, min(1.0, seconds / 10), seconds / 2)
     finally:
         oracle.set_num_threads(cores)
-    return {"value": reps * w.N / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"the whole {w.name} workload ({w.N} tokens), {reps} passes of route+dispatch+permute+"
+    return {"value": reps * T / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the first {T} of the {w.N} tokens of {w.name}, {reps} passes of route+dispatch+permute+"
                       f"combine in fp64 C, {el:.1f} s",
-            "single_thread": {"value": reps1 * w.N / el1, "unit": UNIT, "cores": 1,
-                              "sample": f"{reps1} passes of the same, {el1:.1f} s"},
+            "single_thread": {"value": reps1 * T1 / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"the first {T1} tokens, {reps1} passes of the same, {el1:.1f} s"},
             "cpu_model": cpu_model()}
 
 
@@ -390,30 +426,38 @@ def torch_naive(Xd, Wd, bd, w: mi.Workload, Y, flush, reps: int = 100):
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the oracle on this machine's host cores, rank 0 only.  Each
+    step is one pass over the first T tokens of the workload, T sized so that the
+    warm-up and timed steps take about REF_BUDGET_S seconds (all N tokens when they fit)."""
     if rank != 0:
         return
     import oracle
     w = mi.WORKLOADS[args.workload]
     X, W, bias = mi.make_workload_inputs(w)
-    Xb, Wb = mi.bf16_bits(X), mi.bf16_bits(W)
-    b = None if bias is None else bias.numpy()
-    Y = oracle.run_path(Xb, Wb, b, w.K, w.renorm, w.fp8)["Y"]
-    R = mi.bf16_bits(residual_rows(w)) if args.residual else None
     ue8m0 = args.scale_format == "ue8m0"
+    kw = dict(ue8m0=ue8m0, ep_size=args.ep_size, stats=args.route_stats)
+    probe = mi.Workload(w.name, min(w.N, 1024), w.H, w.E, w.K, w.renorm, w.fp8, w.skew)
+    pXb, pWb, pb, pY = oracle_sample(probe, probe.N, X, W, bias)
+    spt = oracle_seconds_per_token(w, pXb, pWb, pb, pY, probe.N, **kw)
+    T = int(max(64, min(w.N, REF_BUDGET_S / max(1, args.steps + args.warmup) / max(spt, 1e-12))))
+    sw = mi.Workload(w.name, T, w.H, w.E, w.K, w.renorm, w.fp8, w.skew)
+    Xb, Wb, b, Y = oracle_sample(sw, T, X, W, bias)
+    R = mi.bf16_bits(residual_rows(w)[:T]) if args.residual else None
     for _ in range(args.warmup):
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, args.ep_size, args.route_stats)
+        oracle_pass(oracle, Xb, Wb, b, sw, Y, R, **kw)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_pass(oracle, Xb, Wb, b, w, Y, R, ue8m0, args.ep_size, args.route_stats)
+        oracle_pass(oracle, Xb, Wb, b, sw, Y, R, **kw)
     el = time.perf_counter() - t0
-    value = args.steps * w.N / el
-    sample = f"the whole {w.name} workload ({w.N} tokens) per step, fp64 C oracle"
+    value = args.steps * T / el
+    sample = (f"the first {T} of the {w.N} tokens of {w.name} per step (all of them when T == N), "
+              "route+dispatch+permute+combine in fp64 C")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": dict(w.as_dict(), **combine_config(args)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "tokens_per_step": T},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -457,7 +501,7 @@ def run_ours(args, rank, world, local):
     moe.lib()
 
     w = mi.WORKLOADS[args.workload]
-    X, W, bias = mi.make_route_inputs(w.N, w.H, w.E, seed=rank, skew=w.skew)  # each rank its own tokens
+    X, W, bias = mi.make_replica_inputs(w, rank)   # each rank its own tokens, one shared gate
     Xd, Wd = X.to(dev), W.to(dev)
     bd = None if bias is None else bias.to(dev)
     N, H, E, K = w.N, w.H, w.E, w.K

@@ -285,6 +285,18 @@ def dispatch_workspace(E: int, device=None, stream=None) -> torch.Tensor:
     return ws
 
 
+def _fresh_workspace(E: int, device, stream) -> torch.Tensor:
+    """The cached workspace of (device, stream, E) with its 256-byte grid-barrier
+    header cleared on `stream` first.  A completed call leaves the counters at
+    zero, but one whose bounded barrier wait ran out (MOE_ERR_TIMEOUT) does not;
+    clearing them before every call keeps such a call from corrupting the next."""
+    ws = dispatch_workspace(E, device, stream)
+    s = torch.cuda.current_stream(ws.device) if stream is None else stream
+    with torch.cuda.stream(s):
+        ws[:256].zero_()
+    return ws
+
+
 def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, fp8: bool = False,
              bf16: bool = True, want_src_slot: bool = True, out: Optional[Dispatch] = None,
              workspace: Optional[torch.Tensor] = None, fused: bool = True, status=None,
@@ -321,7 +333,7 @@ def dispatch(topk_idx: torch.Tensor, E: int, X: Optional[torch.Tensor] = None, f
     if not fused:
         workspace = None
     elif workspace is None:
-        workspace = dispatch_workspace(E, dev, stream)
+        workspace = _fresh_workspace(E, dev, stream)
     has_x = X is not None
     code = lib().moe_dispatch_ex(
         _ptr(topk_idx), _ptr(X), N, H, E, K, _ptr(out.expert_counts), _ptr(out.expert_offsets),
@@ -361,7 +373,7 @@ def route_dispatch(X: torch.Tensor, W_gate: torch.Tensor, K: int, bias: Optional
             X_perm=torch.empty((N * K, H), dtype=torch.bfloat16, device=dev) if permute else None,
         )
     if workspace is None:
-        workspace = dispatch_workspace(E, dev, stream)
+        workspace = _fresh_workspace(E, dev, stream)
     launches = ctypes.c_int(0)
     code = lib().moe_route_dispatch(
         _ptr(X), _ptr(W_gate), _ptr(bias), N, H, E, K, int(bool(renorm)), _ptr(topk_idx), _ptr(topk_w),
@@ -412,7 +424,7 @@ def dispatch_ep(topk_idx: torch.Tensor, E: int, ep_size: int, X: Optional[torch.
         send_meta=torch.empty((R, P + 1), **i32),
         X_send=torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if X is not None else None)
     if workspace is None:
-        workspace = dispatch_workspace(E, dev, stream)
+        workspace = _fresh_workspace(E, dev, stream)
     code = lib().moe_dispatch_ep(
         _ptr(topk_idx), _ptr(X), N, H, E, K, ep_size, _ptr(out.expert_counts), _ptr(out.expert_offsets),
         _ptr(out.row_map), _ptr(out.rank_counts), _ptr(out.rank_offsets), _ptr(out.send_token),

@@ -59,16 +59,19 @@ extern "C" MOE_API moe_status moe_dispatch_noalloc(const int32_t *topk_idx, cons
                                                    float *X_scale, int32_t *status_word, moe_stream_t stream)
 {
     NvtxRange nvtx_range("moe_dispatch_noalloc");
-    // The same argument checks as moe_dispatch, which then runs with this
-    // library's own scratch as its workspace.
-    if (E < 1 || E > 256 || K < 1 || K > 16 || K > E || N < 0) return MOE_ERR_INVALID_ARG;
-    if (N == 0 || !expert_counts || !expert_offsets || !topk_idx || !row_map)
+    // Every argument check of moe_dispatch runs first, on the host: a rejected
+    // call makes no CUDA call and queues nothing on the stream.
+    const moe_status st = dispatch_check(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map, src_slot,
+                                         X_perm, X_fp8, X_scale, MOE_SCALE_FP32, status_word, nullptr, 0);
+    if (st != MOE_OK) return st;
+    if (N == 0)   // zero counts and offsets; no scratch needed
         return moe_dispatch(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map, src_slot, X_perm, X_fp8,
                             X_scale, status_word, nullptr, 0, stream);
     int dev = 0;
     if (const cudaError_t ge = cudaGetDevice(&dev); ge != cudaSuccess) return from_cuda(ge);
-    // Sizes beyond what the built-in scratch serves: one launch takes at most
-    // one CTA per SM and 16384 slots per CTA.
+    // Sizes beyond what the built-in scratch serves: one launch takes
+    // min(N, SMs) CTAs and at most 16384 slots per CTA, i.e.
+    // ceil(N / min(N, SMs)) * K <= 16384.
     const int64_t sms = device_sm_count(dev);
     const int64_t ctas = N < sms ? N : sms;
     const int64_t tok_per = (N + ctas - 1) / ctas;

@@ -196,13 +196,16 @@ static moe_status validate_permute(const void *X, const int32_t *row_map, int64_
 
 }  // extern "C"
 
-// moe_dispatch_ex; *launches receives the number of kernels launched.
-static moe_status dispatch_impl(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
-                                int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
-                                void *X_perm, void *X_fp8, void *X_scale, int scale_format, int32_t *status_word,
-                                void *workspace, size_t workspace_bytes, cudaStream_t s, int *launches)
+namespace moe {
+
+// Host checks of moe_dispatch_ex's arguments; no CUDA call.  A NULL workspace
+// with workspace_bytes == 0 is valid (the path without workspace).
+moe_status dispatch_check(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                          const int32_t *expert_counts, const int32_t *expert_offsets, const int32_t *row_map,
+                          const int32_t *src_slot, const void *X_perm, const void *X_fp8, const void *X_scale,
+                          int scale_format, const int32_t *status_word, const void *workspace,
+                          size_t workspace_bytes)
 {
-    *launches = 0;
     moe_status st = check_topk(E, K);
     if (st != MOE_OK) return st;
     if ((st = check_rows(N, K)) != MOE_OK) return st;
@@ -222,6 +225,23 @@ static moe_status dispatch_impl(const int32_t *topk_idx, const void *X, int64_t 
         if (X && (st = validate_permute(X, row_map, N, H, K, X_perm, X_fp8, X_scale, scale_format)) != MOE_OK)
             return st;
     }
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+// moe_dispatch_ex; *launches receives the number of kernels launched.
+static moe_status dispatch_impl(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                                int32_t *expert_counts, int32_t *expert_offsets, int32_t *row_map, int32_t *src_slot,
+                                void *X_perm, void *X_fp8, void *X_scale, int scale_format, int32_t *status_word,
+                                void *workspace, size_t workspace_bytes, cudaStream_t s, int *launches)
+{
+    *launches = 0;
+    const moe_status st = dispatch_check(topk_idx, X, N, H, E, K, expert_counts, expert_offsets, row_map, src_slot,
+                                         X_perm, X_fp8, X_scale, scale_format, status_word, workspace,
+                                         workspace_bytes);
+    if (st != MOE_OK) return st;
+    const bool use_ws = workspace != nullptr || workspace_bytes != 0;
     const int ue8m0 = scale_format == MOE_SCALE_UE8M0;
     if (N == 0) {
         // no tokens: every count and offset is zero

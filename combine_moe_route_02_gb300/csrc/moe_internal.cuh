@@ -407,6 +407,14 @@ inline moe_status from_cuda(cudaError_t e)
     return MOE_ERR_CUDA;
 }
 
+// Host checks of moe_dispatch_ex's arguments (moe_api.cu); no CUDA call.  A
+// NULL workspace with workspace_bytes == 0 is valid (the path without workspace).
+moe_status dispatch_check(const int32_t *topk_idx, const void *X, int64_t N, int H, int E, int K,
+                          const int32_t *expert_counts, const int32_t *expert_offsets, const int32_t *row_map,
+                          const int32_t *src_slot, const void *X_perm, const void *X_fp8, const void *X_scale,
+                          int scale_format, const int32_t *status_word, const void *workspace,
+                          size_t workspace_bytes);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count(int device);
 int device_cc_major(int device);

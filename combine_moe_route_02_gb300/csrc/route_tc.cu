@@ -513,21 +513,23 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // The split-K exchange writes into the shared memory of the other CTAs of the
+    // cluster, so it runs only in clusters of the planned nsplit CTAs.  A launch
+    // whose clusters were dropped (a profiler may run a cooperative cluster launch
+    // with clusters of one CTA) runs "solo" instead: each CTA takes the whole H
+    // range of its tile and finishes its own kBM / nsplit tokens, with no peer
+    // memory touched.  The cluster size is the same for every CTA, so all of them
+    // take the same branch before any barrier.
+    bool solo = false;
     if constexpr (SPLIT) {
-        // The split-K exchange writes into the shared memory of the other CTAs of
-        // the cluster: run only as planned, in clusters of nsplit CTAs (the same
-        // for every CTA, so all of them return together before any barrier)
         uint32_t ncta;
         asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
-        if (ncta != static_cast<uint32_t>(p.nsplit)) {
-            if (threadIdx.x == 0) report_status(p.status, MOE_ERR_UNSUPPORTED);
-            return;
-        }
+        solo = ncta != static_cast<uint32_t>(p.nsplit);
     }
-    const uint32_t rank = SPLIT ? cluster_rank() : 0u;
+    const uint32_t rank = SPLIT ? (solo ? blockIdx.x : cluster_rank()) : 0u;
     const int nk = (p.H + kBK - 1) / kBK;
-    const int kb0 = SPLIT ? static_cast<int>(rank) * p.kb_per : 0;
-    const int kb1 = SPLIT ? min(nk, kb0 + p.kb_per) : nk;
+    const int kb0 = SPLIT && !solo ? static_cast<int>(rank) * p.kb_per : 0;
+    const int kb1 = SPLIT && !solo ? min(nk, kb0 + p.kb_per) : nk;
     const int nkb = kb1 > kb0 ? kb1 - kb0 : 0;    // K-steps of this CTA per tile (0: contributes nothing)
     const int first_tile = SPLIT ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
     const int tile_step = SPLIT ? p.tiles : static_cast<int>(gridDim.x);  // split: exactly one tile
@@ -803,8 +805,11 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
             const int row = q * 32 + lane;
             const int nph = p.NP >> 1;
             const uint32_t owner = static_cast<uint32_t>(row / R);
-            const uint32_t local = smem_u32(buf + (static_cast<int>(rank) * R + row % R) * RS);
-            const uint32_t remote = dsmem_map(local, owner);
+            // solo: the CTA's own rows go to slice 0 of its own staging area (the
+            // shared::cta address of an own-CTA location is valid for st.shared::cluster)
+            const uint32_t local = smem_u32(buf + ((solo ? 0 : static_cast<int>(rank)) * R + row % R) * RS);
+            const uint32_t remote = solo ? local : dsmem_map(local, owner);
+            const bool send = !solo || owner == rank;   // (the TMEM loads stay warp-wide)
             const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
             int c = h * nph;
 #pragma unroll 1
@@ -812,16 +817,21 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                 float v[32];
                 tmem_ld_32x32b_x32(lane_addr + c, v);
                 tmem_ld_wait();
+                if (send) {
 #pragma unroll
-                for (int g = 0; g < 32; g += 4) st_dsmem_v4(remote + (c + g) * 4, v[g], v[g + 1], v[g + 2], v[g + 3]);
+                    for (int g = 0; g < 32; g += 4)
+                        st_dsmem_v4(remote + (c + g) * 4, v[g], v[g + 1], v[g + 2], v[g + 3]);
+                }
             }
 #pragma unroll 1
             for (; c < h * nph + nph; c += 8) {
                 float v[8];
                 tmem_ld_32x32b_x8(lane_addr + c, v);
                 tmem_ld_wait();
-                st_dsmem_v4(remote + c * 4, v[0], v[1], v[2], v[3]);
-                st_dsmem_v4(remote + c * 4 + 16, v[4], v[5], v[6], v[7]);
+                if (send) {
+                    st_dsmem_v4(remote + c * 4, v[0], v[1], v[2], v[3]);
+                    st_dsmem_v4(remote + c * 4 + 16, v[4], v[5], v[6], v[7]);
+                }
             }
         }
         tc_fence_before_sync();
@@ -833,7 +843,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
             const int lrow = t / G;
             const int part = t % G;
             const int n = first_tile * p.tile_rows + static_cast<int>(rank) * R + lrow;
-            const int nslices = min(S, (nk + p.kb_per - 1) / p.kb_per);  // CTAs that had K-steps
+            // CTAs that had K-steps (solo: this CTA alone, over all of H)
+            const int nslices = solo ? 1 : min(S, (nk + p.kb_per - 1) / p.kb_per);
             const float *rowbuf = buf + lrow * RS;
             const int sstride = R * RS;                 // floats between the slices of a row
             // this thread's columns part, part + G, ...: eight per step with the loads
@@ -1209,16 +1220,27 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     cfg.numAttrs = na;
     if (fz) {
         // all CTAs resident at once: the grid barrier of the dispatch part cannot
-        // deadlock.  MOE_FUSED_LAUNCH=noncooperative drops the attribute (for
-        // profilers that run cooperative cluster launches without clusters); the
-        // one-wave check above still places every CTA at once on an idle GPU.
-        static const bool noncoop = [] {
+        // deadlock.  MOE_FUSED_LAUNCH (read once per process) changes the launch:
+        //  "noncooperative": without the cooperative attribute (profilers run
+        //      cooperative cluster launches without clusters; a plain cluster launch
+        //      keeps them); the one-wave check above still places every CTA at once
+        //      on an idle GPU;
+        //  "nocluster": cooperative but without the cluster dimension, so that every
+        //      CTA runs the kernel's solo branch, as under such a profiler (a test
+        //      switch for that branch).
+        static const int mode = [] {
             const char *v = std::getenv("MOE_FUSED_LAUNCH");
-            return v != nullptr && std::strcmp(v, "noncooperative") == 0;
+            if (v != nullptr && std::strcmp(v, "noncooperative") == 0) return 1;
+            if (v != nullptr && std::strcmp(v, "nocluster") == 0) return 2;
+            return 0;
         }();
         attr[na].id = cudaLaunchAttributeCooperative;
         attr[na].val.cooperative = 1;
-        cfg.numAttrs = noncoop ? na : na + 1;
+        cfg.numAttrs = mode == 1 ? na : na + 1;
+        if (mode == 2) {   // drop the cluster dimension (attr[0])
+            cfg.attrs = attr + 1;
+            cfg.numAttrs = na;
+        }
         err = cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, true, true>, tmX, tmW, q);
         if (err != cudaSuccess) {
             (void)cudaGetLastError();   // not launched: the caller routes and dispatches apart

@@ -130,9 +130,11 @@ MOE_API moe_status moe_route_stats(const void *X, const void *W_gate, const floa
  *              sorted counts at position 0.95 * (E - 1)
  *   stats[2] = z_coef * (1/N) * sum_n lse[n]^2      (0 if lse is NULL or N == 0)
  *   stats[3] = mean = sum_e counts[e] / E
- * The ratios are 0 when every count is 0.  The sums are taken in fp64 in a
- * fixed order (deterministic).  counts int32 [E] (1 <= E <= 256), lse fp32 [N]
- * or NULL, stats fp32 [4] (all device memory).
+ * The ratios are 0 when every count is 0.  The sum of lse^2 is deterministic:
+ * each of 1024 threads sums a fixed set of the squares in a fixed order in
+ * Kahan-compensated fp32, and the 1024 per-thread sums are then added in fp64
+ * in a fixed order; the count sums are exact integers.  counts int32 [E]
+ * (1 <= E <= 256), lse fp32 [N] or NULL, stats fp32 [4] (all device memory).
  * Errors: MOE_ERR_INVALID_ARG (NULL counts or stats, E out of range, N < 0),
  * MOE_ERR_MISALIGNED, MOE_ERR_CUDA.
  */
@@ -303,9 +305,12 @@ MOE_API moe_status moe_dispatch_ep(const int32_t *topk_idx, const void *X,
  *  - Every call clears the array's barrier counters on `stream` and then uses
  *    the whole array: calls that may overlap on the GPU (other streams, other
  *    host threads) race on it and must be serialised by the caller.
- *  - Limit: one CTA per SM and at most 16384 slots per CTA, i.e.
- *    N*K <= 16384 * (number of SMs) (about 2.49 million slots on a 152-SM
- *    GB300); larger calls return MOE_ERR_UNSUPPORTED and launch nothing.
+ *  - Limit: the launch takes C = min(N, number of SMs) CTAs, each with
+ *    ceil(N / C) tokens, and a CTA holds at most 16384 slots, so the call
+ *    needs ceil(N / C) * K <= 16384 (on a 152-SM GB300 with K = 3: up to
+ *    N = 830072); larger calls return MOE_ERR_UNSUPPORTED and launch nothing.
+ *  - Every argument check of moe_dispatch runs on the host before any CUDA
+ *    call: a rejected call queues nothing on `stream`.
  */
 MOE_API moe_status moe_dispatch_noalloc(const int32_t *topk_idx, const void *X,
                                 int64_t N, int H, int E, int K,

@@ -61,8 +61,9 @@ WORKLOADS = {
     ]
 }
 
-# The workload the benchmark times by default.
-BENCH_WORKLOAD = "n2048_h1024_e64_k2"
+# The workload the benchmark times by default: the largest of the five, the one
+# that fits a single GPU and where the copy and router kernels run at HBM speed.
+BENCH_WORKLOAD = "skewed_zipf_n65536_h4096_e64_k2"
 
 
 def zipf_bias(E: int) -> torch.Tensor:
@@ -82,6 +83,20 @@ def make_route_inputs(N: int, H: int, E: int, seed: int = 0, skew: bool = False)
 
 def make_workload_inputs(w: Workload, seed: int | None = None):
     return make_route_inputs(w.N, w.H, w.E, w.seeds[0] if seed is None else seed, w.skew)
+
+
+def make_replica_inputs(w: Workload, rank: int):
+    """Inputs of one data-parallel replica: rank r routes its own tokens (the X
+    drawn from a generator seeded with seed0 + r) against the gate every rank
+    shares (the W drawn from the seed0 generator, after its X).  Rank 0's inputs
+    are the workload's own."""
+    seed0 = w.seeds[0]
+    X0, W, bias = make_route_inputs(w.N, w.H, w.E, seed0, w.skew)
+    if rank == 0:
+        return X0, W, bias
+    del X0
+    X, _, _ = make_route_inputs(w.N, w.H, w.E, seed0 + rank, w.skew)
+    return X, W, bias
 
 
 def random_topk_idx(N: int, E: int, K: int, seed: int = 0) -> torch.Tensor:

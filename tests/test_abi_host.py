@@ -169,6 +169,39 @@ def test_route_dispatch_validation(L):
     assert route_dispatch(L, src=A + 2) == MISALIGNED
 
 
+def noalloc_fn(L):
+    f = L.moe_dispatch_noalloc
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    f.argtypes = [P, P, I64, I32, I32, I32, P, P, P, P, P, P, P, P, P]
+    f.restype = I32
+    return f
+
+
+def noalloc(L, idx=A, X=None, N=16, H=64, E=16, K=2, counts=A2, offsets=A3, row_map=A4,
+            src=None, xp=None, xq=None, xs=None, st=None):
+    return noalloc_fn(L)(idx, X, N, H, E, K, counts, offsets, row_map, src, xp, xq, xs, st, None)
+
+
+def test_noalloc_validation(L):
+    # moe_dispatch_noalloc runs moe_dispatch's argument checks before any CUDA
+    # call: on this machine (no GPU) any CUDA call would fail with MOE_ERR_CUDA,
+    # so each code below also shows that nothing reached CUDA or a stream
+    assert noalloc(L, idx=A + 2) == MISALIGNED
+    assert noalloc(L, row_map=A4 + 2) == MISALIGNED
+    assert noalloc(L, st=A + 2) == MISALIGNED
+    assert noalloc(L, X=A, xp=A2 + 4) == MISALIGNED
+    assert noalloc(L, X=A + 8, xp=A2) == MISALIGNED
+    assert noalloc(L, X=A, H=12, xp=A) == MISALIGNED
+    assert noalloc(L, X=A, H=128, xq=A, xs=A2 + 2) == MISALIGNED   # fp32 scales need 4-byte alignment
+    assert noalloc(L, E=0) == INVALID
+    assert noalloc(L, K=17, E=32) == INVALID
+    assert noalloc(L, N=-1) == INVALID
+    assert noalloc(L, counts=None) == INVALID
+    assert noalloc(L, idx=None) == INVALID
+    assert noalloc(L, xp=A) == INVALID                           # output rows without X
+    assert noalloc(L, X=A, H=192, xq=A, xs=A2) == INVALID        # H % 128 != 0
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
 def test_valid_call_without_gpu_fails_loudly(L):
     # arguments pass validation, then the first CUDA call fails: MOE_ERR_CUDA, no crash
@@ -180,6 +213,8 @@ def test_valid_call_without_gpu_fails_loudly(L):
                                 L.moe_dispatch_workspace_size(16, 16, 2), None, None) == CUDA
     # UE8M0 scale bytes need no alignment: the call passes validation (then fails on CUDA)
     assert L.moe_permute_ex(A, A2, 8, 128, 2, A3, A4, A + 2, 1, None, None) == CUDA
+    # a valid no-allocation dispatch reaches its first CUDA call only after the checks
+    assert noalloc(L) == CUDA
 
 
 def test_binding_refuses_cpu_tensors():

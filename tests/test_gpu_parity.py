@@ -851,6 +851,48 @@ def test_random_shapes_whole_path_match_oracle(N, H, E, K, skew, renorm):
     combine_close(bits(out), ref)
 
 
+def test_route_dispatch_solo_branch_in_a_child_process():
+    # MOE_FUSED_LAUNCH=nocluster launches the one route + dispatch kernel cooperatively
+    # but without its cluster dimension, as a profiler may run it: every CTA then takes
+    # the kernel's solo branch (the whole H range of its tile, its own tokens, no
+    # distributed shared memory).  The results must still match the oracle: the ids and
+    # weights within the route tolerance, the dispatch of those ids and the rows bit-exact.
+    import subprocess
+    import sys
+    code = (
+        "import numpy as np, torch, combine_moe_route_02_gb300 as moe, moe_inputs as mi, oracle\n"
+        "from parity_util import compare_topk\n"
+        "moe.lib()\n"
+        "bits = lambda t: mi.bf16_bits(t.cpu())\n"
+        "for (N, H, E, K, skew) in [(2048, 1024, 64, 2, False), (512, 256, 16, 2, False),\n"
+        "                           (4096, 512, 64, 4, False), (777, 512, 32, 3, True),\n"
+        "                           (600, 2048, 256, 8, False), (130, 2048, 256, 16, False),\n"
+        "                           (9000, 256, 64, 2, False), (300, 7168, 64, 2, False)]:\n"
+        "    X, W, bias = mi.make_route_inputs(N, H, E, N + H + K, skew=skew)\n"
+        "    renorm = not skew\n"
+        "    st = torch.zeros(1, dtype=torch.int32, device='cuda')\n"
+        "    idx, tw, d, n = moe.route_dispatch(X.cuda(), W.cuda(), K, None if bias is None else bias.cuda(),\n"
+        "                                       renorm, status=st)\n"
+        "    torch.cuda.synchronize()\n"
+        "    assert st.item() == 0 and n == 1, (N, H, E, K, st.item(), n)\n"
+        "    r_idx, r_w, L, P = oracle.route(bits(X), bits(W), None if bias is None else bias.numpy(), K,\n"
+        "                                    renorm, want_logits=True, want_probs=True)\n"
+        "    gi = idx.cpu().numpy()\n"
+        "    compare_topk(gi, tw.cpu().numpy(), r_idx, r_w, L, P, renorm)\n"
+        "    c, o, r, s = oracle.dispatch(gi, E)\n"
+        "    assert np.array_equal(d.expert_counts.cpu().numpy(), c)\n"
+        "    assert np.array_equal(d.expert_offsets.cpu().numpy(), o)\n"
+        "    assert np.array_equal(d.row_map.cpu().numpy(), r)\n"
+        "    assert np.array_equal(d.src_slot.cpu().numpy(), s)\n"
+        "    assert np.array_equal(bits(d.X_perm), oracle.permute(bits(X), r, K))\n"
+        "print('ok')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MOE_FUSED_LAUNCH="nocluster",
+               PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert out.returncode == 0 and out.stdout.strip().endswith("ok"), out.stderr[-3000:]
+
+
 def test_route_dispatch_noncooperative_launch_in_a_child_process():
     # MOE_FUSED_LAUNCH=noncooperative (read once per process): the same one launch without the
     # cooperative attribute gives the same results

@@ -1,6 +1,6 @@
 """The multi-rank (torchrun) host logic of bench.py on CPU with the gloo
-backend, world size 2: each rank routes its own tokens (distinct seeds), the
-job time is the max over ranks, throughput scales with the number of ranks
+backend, world size 2: each rank routes its own tokens (distinct seeds)
+against one shared gate weight, the job time is the max over ranks, throughput scales with the number of ranks
 (weak scaling), and the load statistics are taken on the expert counts of all
 ranks added up.  No GPU and no collective on the data path."""
 import os
@@ -26,11 +26,13 @@ def _rank_main(rank, world, port, q):
     try:
         local_ms = [10.0, 25.0][rank]                     # rank 1 is the slow one
         total = bench.max_over_ranks(local_ms, dist, "cpu")
-        X, _, _ = mi.make_route_inputs(64, 32, 8, seed=rank)  # the seed bench.py gives each rank
-        digest = float(X.float().sum())
-        digests = [None] * world
-        dist.all_gather_object(digests, digest)
-        q.put((rank, total, bench.weak_scaling_tokens_per_s(world, 2048, 100, total), digests))
+        # the inputs bench.py gives each rank: its own tokens, the shared gate
+        X, W, bias = mi.make_replica_inputs(mi.Workload("t", 64, 32, 8, 2, skew=True), rank)
+        mine = (X.view(torch.int16).numpy().tobytes(), W.view(torch.int16).numpy().tobytes(),
+                bias.numpy().tobytes())
+        every = [None] * world
+        dist.all_gather_object(every, mine)
+        q.put((rank, total, bench.weak_scaling_tokens_per_s(world, 2048, 100, total), every))
     finally:
         dist.destroy_process_group()
 
@@ -47,10 +49,24 @@ def test_two_gloo_ranks_take_max_time_and_own_tokens():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    for rank, total, value, digests in results:
+    for rank, total, value, every in results:
         assert total == 25.0                              # max over ranks
         assert value == pytest.approx(2 * 2048 * 100 / 0.025)
-        assert digests[0] != digests[1]                   # different tokens per rank
+        assert every[0][0] != every[1][0]                 # different tokens per rank
+        assert every[0][1] == every[1][1]                 # one gate weight, bit for bit
+        assert every[0][2] == every[1][2]                 # and one bias
+
+
+def test_replica_inputs_of_rank_zero_are_the_workloads_own():
+    import moe_inputs as mi
+    w = mi.Workload("t", 48, 16, 8, 2)
+    X0, W0, _ = mi.make_workload_inputs(w)
+    X, W, _ = mi.make_replica_inputs(w, 0)
+    assert torch.equal(X.view(torch.int16), X0.view(torch.int16))
+    assert torch.equal(W.view(torch.int16), W0.view(torch.int16))
+    X1, W1, _ = mi.make_replica_inputs(w, 1)
+    assert torch.equal(W1.view(torch.int16), W0.view(torch.int16))
+    assert not torch.equal(X1.view(torch.int16), X0.view(torch.int16))
 
 
 def test_single_rank_needs_no_process_group():
