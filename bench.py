@@ -58,6 +58,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=mi.BENCH_WORKLOAD, choices=sorted(mi.WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--tokens", type=int, default=0,
+                   help="run the workload's shape with this many tokens instead of its N (for profiler "
+                        "captures on a smaller case; the line then names the workload NAME@N=T)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -826,7 +829,7 @@ def run_ours(args, rank, world, local):
             "frac": kern[dom]["gbs"] / peak, "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
             if peak_src == "measured" else "fallback 6800 GB/s",
             "traffic": ncu_traffic(dom, w.name), "algorithmic_bytes_per_launch": kb[dom],
-            "traffic_source": "profiles/dram_traffic.md (ncu dram__bytes_read.sum + dram__bytes_write.sum per "
+            "traffic_source": "profiles/dram_traffic.csv (ncu dram__bytes_read.sum + dram__bytes_write.sum per "
                               "launch; null when absent or taken on an older source of the kernel)"}
 
     line = {
@@ -870,6 +873,12 @@ def run_ours(args, rank, world, local):
 
 def main():
     args = parse_args()
+    if args.tokens:
+        import dataclasses
+        w = mi.WORKLOADS[args.workload]
+        name = f"{w.name}@N={args.tokens}"
+        mi.WORKLOADS[name] = dataclasses.replace(w, name=name, N=args.tokens)
+        args.workload = name
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)

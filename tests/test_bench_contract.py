@@ -86,8 +86,30 @@ def test_gpu_line_has_the_contract_keys():
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(c)
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    # the bench workload fuses route and dispatch into one launch: two kernels per step
-    assert d["gpu_launches"] >= 2 * d["steps"]
+    # the default workload is the largest one: route, the dispatch's metadata launch,
+    # the row copy in a launch of its own (>= 256 MiB) and the combine
+    import moe_inputs as mi
+    assert d["config"]["workload"] == mi.BENCH_WORKLOAD == "skewed_zipf_n65536_h4096_e64_k2"
+    assert d["gpu_launches"] == 4 * d["steps"]
+    assert d["roofline"]["kernel"] in ("route", "dispatch", "combine")
+    assert d["roofline"]["traffic_source"].startswith("profiles/dram_traffic.csv")
+
+
+@pytest.mark.gpu
+def test_gpu_line_of_the_fused_workload():
+    # at N=2048, H=1024 the router runs split-K and route + dispatch is one launch:
+    # two kernels per step
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "n2048_h1024_e64_k2", "--steps", "5",
+           "--warmup", "3", "--no-cpu-baseline", "--e2e-steps", "16", "--no-torch-naive"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["gpu_launches"] == 2 * d["steps"]
     assert "route_dispatch" in d["kernels"] and d["kernels"]["route_dispatch"]["launches"] == 1
     assert d["roofline"]["kernel"] in ("route_dispatch", "combine")
 
