@@ -53,9 +53,22 @@ namespace {
 
 constexpr int kBM = 128;                       // tokens per tile (UMMA M)
 constexpr int kBK = 64;                        // bf16 per 128-byte swizzle row (one K-step)
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 8;                   // split mode (and the dispatch tail fused into it)
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // 320
 constexpr int kWarps = kThreads / 32;
+
+// Epilogue width per mode: 8 warps, two per TMEM lane quarter, so each token's
+// columns are split into two parts in persistent mode.  (The persistent
+// epilogue is written for 2 or 4 parts; 16 warps with four parts measured no
+// faster on GB300 at E = 128, K = 8: the candidate loop is bound by its
+// instruction count, not by latency, and the extra merge level cost more than
+// the shorter scans saved.)
+template <int KMAX, bool SPLIT>
+struct TcShape {
+    static constexpr int kEpi = kEpiWarps;
+    static constexpr int kThr = 64 + 32 * kEpi;
+    static constexpr int kParts = kEpi / 4;       // column parts per token (persistent mode)
+};
 // rows of the per-CTA count table in the dispatch workspace: the same bound as the
 // dispatch kernel's table (dispatch.cu), which sizes moe_dispatch_workspace_size()
 constexpr int kFuseMaxCtas = 1024;
@@ -107,12 +120,12 @@ struct TcParams {
 // 16-byte aligned for vector DSMEM stores and spreads banks.
 __host__ __device__ constexpr int stage_row_floats(int NP) { return NP + 4; }
 
-// Epilogue exchange area (persistent mode): per column half a sorted list per
+// Epilogue exchange area (persistent mode): per column part a sorted list per
 // token (KMAX keys + KMAX ids) and the running (max, sum-exp); then, in both
 // modes, per token the final K logits.
-__host__ __device__ constexpr uint32_t exch_lists_bytes(int kmax)
+__host__ __device__ constexpr uint32_t exch_lists_bytes(int kmax, int nparts)
 {
-    return static_cast<uint32_t>(2 * kBM * kmax * 8 + 2 * kBM * 2 * 4);
+    return static_cast<uint32_t>(nparts * kBM * kmax * 8 + nparts * kBM * 2 * 4);
 }
 __host__ __device__ constexpr uint32_t win_bytes(int kmax) { return static_cast<uint32_t>(kBM * kmax * 4); }
 
@@ -186,6 +199,45 @@ __device__ __forceinline__ float logit_of(float acc, float bias)
 {
     const float x = acc + bias;
     return isnan(x) ? -INFINITY : x;
+}
+
+// The logit acc + bias with NaN as -inf, and its order key, for a bias that is
+// never -0 (the kernel stores bias + 0.0f): then the sum is never -0 either (in
+// round-to-nearest a sum is -0 only when both terms are), so the key needs no
+// sign-of-zero fix, and fmaxf(NaN, -inf) = -inf takes care of NaN.
+__device__ __forceinline__ float canon_logit(float acc, float bias_canon)
+{
+    return fmaxf(acc + bias_canon, -INFINITY);
+}
+
+__device__ __forceinline__ int canon_key(float x)
+{
+    const int b = __float_as_int(x);
+    return b ^ ((b >> 31) & 0x7FFFFFFF);
+}
+
+// Merge two sorted top-K lists held in shared memory (keys and ids at a stride
+// of kBM ints) into the first K entries of registers: K rounds of "take the
+// better head", equal keys to the lower id.
+template <int KMAX>
+__device__ __forceinline__ void merge2_to_regs(const int *ka_s, const int *ia_s, const int *kb_s, const int *ib_s, int K,
+                                               int (&k)[KMAX], int (&ix)[KMAX])
+{
+    int pa = 0, pb = 0;
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+        if (t < K) {
+            const int ka = pa < K ? ka_s[pa * kBM] : kKeyEmpty;
+            const int ia = pa < K ? ia_s[pa * kBM] : kEmpty;
+            const int kb = pb < K ? kb_s[pb * kBM] : kKeyEmpty;
+            const int ib = pb < K ? ib_s[pb * kBM] : kEmpty;
+            const bool take_b = ranks_above(kb, ib, ka, ia);
+            k[t] = take_b ? kb : ka;
+            ix[t] = take_b ? ib : ia;
+            pa += take_b ? 0 : 1;
+            pb += take_b ? 1 : 0;
+        }
+    }
 }
 
 // Online max / sum of exp over the logits a thread sees (renorm off, or the
@@ -488,11 +540,14 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
 }
 
 template <int KMAX, bool SPLIT, bool FUSE = false>
-__global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                               const __grid_constant__ CUtensorMap tmW,
-                                                               const TcParams p)
+__global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
+    route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const TcParams p)
 {
     static_assert(SPLIT || !FUSE, "the dispatch tail takes its ids from the split-mode epilogue");
+    constexpr int EPW = TcShape<KMAX, SPLIT>::kEpi;    // epilogue warps
+    constexpr int NT = TcShape<KMAX, SPLIT>::kThr;     // threads of the CTA
+    constexpr int NPART = TcShape<KMAX, SPLIT>::kParts;
+    static_assert(!FUSE || NT == kThreads, "the dispatch tail is written for the split-mode CTA");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms, as an offset from the
     // shared array: a pointer derived this way keeps its shared address space,
@@ -506,9 +561,9 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
     float *bias_s = reinterpret_cast<float *>(&tail + 1);
     int *hist_s = reinterpret_cast<int *>(bias_s + p.EP);                // [EP] selections per expert
     // exchange area, token-minor so that the lanes of a warp touch consecutive words
-    int *lst_k = reinterpret_cast<int *>(smem + p.exch_off);            // [2 halves][KMAX][128] keys
-    int *lst_i = lst_k + 2 * kBM * KMAX;                                   // [2 halves][KMAX][128] ids
-    float *lst_rz = reinterpret_cast<float *>(lst_i + 2 * kBM * KMAX);     // [2 halves][2][128]
+    int *lst_k = reinterpret_cast<int *>(smem + p.exch_off);            // [NPART][KMAX][128] keys
+    int *lst_i = lst_k + NPART * kBM * KMAX;                               // [NPART][KMAX][128] ids
+    float *lst_rz = reinterpret_cast<float *>(lst_i + NPART * kBM * KMAX); // [NPART][2][128]
     float *win_v = reinterpret_cast<float *>(smem + p.win_off);            // [KMAX][128]
 
     const int warp = threadIdx.x >> 5;
@@ -544,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tail.acc_full[b], 1);
-            mbar_init(&tail.acc_empty[b], kEpiWarps);
+            mbar_init(&tail.acc_empty[b], EPW);
         }
         mbar_init(&tail.drain, 1);
         tail.abort = 0;
@@ -576,11 +631,12 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
     pdl_wait_prior_grids();
     if (warp != 0) {
         // the producer starts streaming at once; the bias is needed by the epilogue only
-        for (int e = threadIdx.x - 32; e < p.EP; e += kThreads - 32) {
-            bias_s[e] = (p.bias != nullptr && e < E) ? p.bias[e] : 0.f;
+        for (int e = threadIdx.x - 32; e < p.EP; e += NT - 32) {
+            // + 0.0f turns a -0 bias into +0 (see canon_logit)
+            bias_s[e] = ((p.bias != nullptr && e < E) ? p.bias[e] : 0.f) + 0.0f;
             hist_s[e] = 0;
         }
-        named_barrier_sync(5, kThreads - 32);
+        named_barrier_sync(7, NT - 32);
     }
 
     bool acc_ok = false;  // split mode, epilogue threads: the partial accumulator is complete
@@ -664,25 +720,25 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
     } else {
         // ------------------------------------------------------------ epilogue warps
         const int q = warp & 3;                // TMEM lane quarter this warp may access
-        const int h = (warp - 2) >> 2;         // which half of the expert columns
+        const int h = (warp - 2) >> 2;         // which part of the expert columns
         const int row = q * 32 + lane;         // token row of the tile (= TMEM lane)
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const int nph = p.NP >> 1;             // columns per half (a multiple of 8)
         if constexpr (!SPLIT) {
+            const int npp = p.NP / NPART;      // columns per part (a multiple of 4)
             int j = 0;
             for (int tile = first_tile; tile < p.tiles; tile += tile_step, ++j) {
                 const int b = j & 1;
                 if (!mbar_wait_bounded(&tail.acc_full[b], (j >> 1) & 1, abort_flag, 64)) break;
                 tc_fence_after_sync();
-                // ---- this half's columns: two interleaved lists for ILP
+                // ---- this part's columns: two interleaved lists for ILP
                 int ak[KMAX], bk[KMAX], ai[KMAX], bi[KMAX];
                 topk_clear<KMAX>(ak, ai);
                 topk_clear<KMAX>(bk, bi);
                 float r = -INFINITY, z = 0.f;
-                const int c_end = min(E, h * nph + nph);
+                const int c_end = min(E, h * npp + npp);
                 const uint32_t col_addr = lane_addr + static_cast<uint32_t>(b * p.NP);
-                int c = h * nph;
-                // 32 columns per TMEM round trip while they lie inside this half
+                int c = h * npp;
+                // 32 columns per TMEM round trip while they lie inside this part, then 8, then 4
 #pragma unroll 1
                 for (; c + 32 <= c_end; c += 32) {
                     float v[32];
@@ -690,10 +746,10 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                     tmem_ld_wait();
 #pragma unroll
                     for (int t = 0; t < 32; t += 2) {
-                        const float x0 = logit_of(v[t], bias_s[c + t]);
-                        const float x1 = logit_of(v[t + 1], bias_s[c + t + 1]);
-                        topk_push<KMAX>(ak, ai, order_key(x0), c + t);
-                        topk_push<KMAX>(bk, bi, order_key(x1), c + t + 1);
+                        const float x0 = canon_logit(v[t], bias_s[c + t]);
+                        const float x1 = canon_logit(v[t + 1], bias_s[c + t + 1]);
+                        topk_push<KMAX>(ak, ai, canon_key(x0), c + t);
+                        topk_push<KMAX>(bk, bi, canon_key(x1), c + t + 1);
                         if (p.need_z) {
                             online_sumexp(x0, r, z);
                             online_sumexp(x1, r, z);
@@ -701,16 +757,32 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                     }
                 }
 #pragma unroll 1
-                for (; c < c_end; c += 8) {
+                for (; c + 8 <= c_end; c += 8) {
                     float v[8];
                     tmem_ld_32x32b_x8(col_addr + c, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int t = 0; t < 8; t += 2) {
-                        const float x0 = logit_of(v[t], bias_s[c + t]);
-                        const float x1 = logit_of(v[t + 1], bias_s[c + t + 1]);
-                        topk_push<KMAX>(ak, ai, order_key(x0), c + t);
-                        topk_push<KMAX>(bk, bi, order_key(x1), c + t + 1);
+                        const float x0 = canon_logit(v[t], bias_s[c + t]);
+                        const float x1 = canon_logit(v[t + 1], bias_s[c + t + 1]);
+                        topk_push<KMAX>(ak, ai, canon_key(x0), c + t);
+                        topk_push<KMAX>(bk, bi, canon_key(x1), c + t + 1);
+                        if (p.need_z) {
+                            online_sumexp(x0, r, z);
+                            online_sumexp(x1, r, z);
+                        }
+                    }
+                }
+                if (c < c_end) {   // a last group of 4 columns (E % 8 == 0, parts start at multiples of 4)
+                    float v[4];
+                    tmem_ld_32x32b_x4(col_addr + c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 4; t += 2) {
+                        const float x0 = canon_logit(v[t], bias_s[c + t]);
+                        const float x1 = canon_logit(v[t + 1], bias_s[c + t + 1]);
+                        topk_push<KMAX>(ak, ai, canon_key(x0), c + t);
+                        topk_push<KMAX>(bk, bi, canon_key(x1), c + t + 1);
                         if (p.need_z) {
                             online_sumexp(x0, r, z);
                             online_sumexp(x1, r, z);
@@ -721,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tail.acc_empty[b]);
-                // ---- merge the two lists into this half's sorted top-K (shared memory)
+                // ---- merge the two lists into this part's sorted top-K (shared memory)
                 int *my_k = lst_k + h * KMAX * kBM + row;
                 int *my_i = lst_i + h * KMAX * kBM + row;
 #pragma unroll 1
@@ -734,14 +806,35 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                 }
                 lst_rz[(h * 2) * kBM + row] = r;
                 lst_rz[(h * 2 + 1) * kBM + row] = z;
-                named_barrier_sync(1 + q, 64);   // both halves' lists are ready
+                named_barrier_sync(1 + q, 32 * NPART);   // every part's list is ready
+                if constexpr (NPART == 4) {
+                    // parts 0 and 2 fold in parts 1 and 3 (written back over their own lists)
+                    if ((h & 1) == 0) {
+                        merge2_to_regs<KMAX>(my_k, my_i, my_k + KMAX * kBM, my_i + KMAX * kBM, K, ak, ai);
+#pragma unroll
+                        for (int t = 0; t < KMAX; ++t)
+                            if (t < K) {
+                                my_k[t * kBM] = ak[t];
+                                my_i[t * kBM] = ai[t];
+                            }
+                        if (p.need_z) {
+                            const float r1 = lst_rz[(h * 2 + 2) * kBM + row], z1 = lst_rz[(h * 2 + 3) * kBM + row];
+                            const float rm = fmaxf(r, r1);
+                            const float zs = (z > 0.f ? z * expf(r - rm) : 0.f) + (z1 > 0.f ? z1 * expf(r1 - rm) : 0.f);
+                            lst_rz[(h * 2) * kBM + row] = rm;
+                            lst_rz[(h * 2 + 1) * kBM + row] = zs;
+                        }
+                    }
+                    named_barrier_sync(1 + q, 32 * NPART);
+                }
                 if (h == 0) {
                     // ---- two-way merge of the halves, K rounds; ids written as selected
+                    constexpr int kOther = NPART / 2;   // the part holding the other half's list
                     const int n = tile * p.tile_rows + row;
                     // rows past tile_rows belong to the next tile (the TMA box is kBM rows)
                     const bool mine = row < p.tile_rows && n < p.N;
-                    const int *ok = lst_k + KMAX * kBM + row;
-                    const int *oi = lst_i + KMAX * kBM + row;
+                    const int *ok = lst_k + kOther * KMAX * kBM + row;
+                    const int *oi = lst_i + kOther * KMAX * kBM + row;
                     float *wrow = win_v + row;
                     int pa = 0, pb = 0;
 #pragma unroll 1
@@ -764,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                     float zfull = 0.f;         // sum over all experts of exp(logit - m)
                     if (p.need_z) {
                         const float r0 = lst_rz[row], z0 = lst_rz[kBM + row];
-                        const float r1 = lst_rz[2 * kBM + row], z1 = lst_rz[3 * kBM + row];
+                        const float r1 = lst_rz[(kOther * 2) * kBM + row], z1 = lst_rz[(kOther * 2 + 1) * kBM + row];
                         zfull = (z0 > 0.f ? z0 * expf(r0 - m) : 0.f) + (z1 > 0.f ? z1 * expf(r1 - m) : 0.f);
                     }
                     float denom = zfull;
@@ -780,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
                         if (p.lse) p.lse[n] = m == -INFINITY ? -INFINITY : m + logf(zfull);
                     }
                 }
-                named_barrier_sync(1 + q, 64);   // the lists have been consumed
+                named_barrier_sync(1 + q, 32 * NPART);   // the lists have been consumed
             }
         } else {
             acc_ok = mbar_wait_bounded(&tail.acc_full[0], 0, abort_flag, 64);
@@ -839,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
         cluster_sync_all();                             // #2: all partial logits delivered
         if (warp >= 2) {
             const int t = threadIdx.x - 64;             // 0..255
-            const int G = (32 * kEpiWarps) / R;         // threads per token: 2S (4, 8 or 16)
+            const int G = (32 * EPW) / R;               // threads per token: 2S (4, 8 or 16)
             const int lrow = t / G;
             const int part = t % G;
             const int n = first_tile * p.tile_rows + static_cast<int>(rank) * R + lrow;
@@ -949,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 2 : 1) route_tc_kernel(const
     __syncthreads();
     if (p.counts) {
         // this CTA's selections per expert, added to the grid-wide counts
-        for (int e = threadIdx.x; e < E; e += kThreads)
+        for (int e = threadIdx.x; e < E; e += NT)
             if (hist_s[e] != 0) atomicAdd(p.counts + e, hist_s[e]);
     }
     if (warp == 1) {
@@ -1015,12 +1108,12 @@ struct TcLayout {
 // the staging area overlays the ring instead (it is written only once every
 // CTA of the cluster has finished its MMAs), for gates so wide that a ring
 // beside it would hold a single stage.
-bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, TcLayout &L)
+bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, TcLayout &L, int nparts = 2)
 {
     const size_t slot = kABytes + static_cast<size_t>(EP) * kBK * 2;
     const size_t staging = split ? static_cast<size_t>(kBM) * stage_row_floats(NP) * sizeof(float) : 0;
     const size_t apart = alias ? 0 : staging;
-    const size_t exch = (split ? 0 : exch_lists_bytes(kmax)) + win_bytes(kmax);
+    const size_t exch = (split ? 0 : exch_lists_bytes(kmax, nparts)) + win_bytes(kmax);
     const size_t fixed = 1024 + apart + exch + sizeof(TcSmemTail) + (sizeof(float) + sizeof(int)) * EP;
     const int max_st = split ? (kb_per < kMaxStages ? (kb_per < 1 ? 1 : kb_per) : kMaxStages) : kMaxStages;
     const int min_st = split ? 1 : 2;
@@ -1035,7 +1128,7 @@ bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, Tc
                 L.alias = alias && split;
                 L.staging_off = static_cast<uint32_t>(alias ? 0 : ring);
                 L.exch_off = static_cast<uint32_t>(ring + apart);
-                L.win_off = static_cast<uint32_t>(ring + apart + (split ? 0 : exch_lists_bytes(kmax)));
+                L.win_off = static_cast<uint32_t>(ring + apart + (split ? 0 : exch_lists_bytes(kmax, nparts)));
                 L.tail_off = static_cast<uint32_t>(ring + apart + exch);
                 L.smem = fixed + ring;
                 return true;
@@ -1077,8 +1170,8 @@ int max_active_clusters(size_t smem, int S, int dev)
     // cached per (device, cluster size, shared memory size)
     static std::mutex mu;
     static std::map<uint64_t, int> cache;
-    const uint64_t key = (static_cast<uint64_t>(FUSE) << 48) | (static_cast<uint64_t>(dev) << 40) |
-                         (static_cast<uint64_t>(S) << 32) | smem;
+    const uint64_t key = (static_cast<uint64_t>(KMAX) << 52) | (static_cast<uint64_t>(FUSE) << 48) |
+                         (static_cast<uint64_t>(dev) << 40) | (static_cast<uint64_t>(S) << 32) | smem;
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -1169,7 +1262,7 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
         }
     }
     if (split ? !split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, L)
-              : !layout_for(q.EP, q.NP, KMAX, false, nk, false, L))
+              : !layout_for(q.EP, q.NP, KMAX, false, nk, false, L, TcShape<KMAX, false>::kParts))
         return cudaErrorInvalidConfiguration;
     q.stages = L.stages;
     q.exch_off = L.exch_off;
@@ -1210,7 +1303,7 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     } else {
         cfg.gridDim = dim3(static_cast<unsigned>(q.tiles < sms ? q.tiles : sms), 1, 1);
     }
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(split ? TcShape<KMAX, true>::kThr : TcShape<KMAX, false>::kThr), 1, 1);
     cfg.dynamicSmemBytes = L.smem;
     cfg.stream = stream;
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
