@@ -127,19 +127,35 @@ __host__ __device__ constexpr uint32_t exch_lists_bytes(int kmax, int nparts)
 {
     return static_cast<uint32_t>(nparts * kBM * kmax * 8 + nparts * kBM * 2 * 4);
 }
-__host__ __device__ constexpr uint32_t win_bytes(int kmax) { return static_cast<uint32_t>(kBM * kmax * 4); }
+// Selection window: per token the K selected logits (then the weights) and the
+// K selected ids, token-minor ([KMAX][128] floats, then [KMAX][128] ints), from
+// which the outputs leave with coalesced stores.
+__host__ __device__ constexpr uint32_t win_bytes(int kmax) { return static_cast<uint32_t>(2 * kBM * kmax * 4); }
 
-// Order-preserving int32 key of a logit: NaN counts as -inf, -0 as +0, and
-// keys compare like the floats.  kKeyEmpty (below the key of -inf) marks an
-// empty list slot.
-constexpr int kKeyEmpty = static_cast<int>(0x80000000u);
-
-__device__ __forceinline__ int order_key(float x)
+// Coalesced copy of `rows` consecutive tokens' K values from a token-minor
+// window (value k of token r at win[k * kBM + r0 + r]) to dst[r * K + k]; the
+// `nthr` threads with rank `t` share the copy.
+template <typename T>
+__device__ __forceinline__ void window_to_global(T *dst, const T *win, int r0, int rows, int K, int t, int nthr)
 {
-    x = isnan(x) ? -INFINITY : x + 0.0f;
-    const int b = __float_as_int(x);
-    return b >= 0 ? b : (b ^ 0x7FFFFFFF);
+    const int total = rows * K;
+    int k = t % K, r = t / K;
+    const int dk = nthr % K, dr = nthr / K;
+    for (int i = t; i < total; i += nthr) {
+        dst[i] = win[k * kBM + r0 + r];
+        k += dk;
+        r += dr;
+        if (k >= K) {
+            k -= K;
+            ++r;
+        }
+    }
 }
+
+// Logits are ranked by an order-preserving int32 key (canon_key below: keys
+// compare like the floats, with NaN taken as -inf and no -0 reaching it).
+// kKeyEmpty (below the key of -inf) marks an empty list slot.
+constexpr int kKeyEmpty = static_cast<int>(0x80000000u);
 
 __device__ __forceinline__ float key_value(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF)); }
 
@@ -329,7 +345,7 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
     constexpr int kIdIters = ((kBM / 2 * KMAX + kWarps - 1) / kWarps + 31) / 32;   // R <= kBM / 2
     int ids[kIdIters];
     {
-        const int *ids_s = reinterpret_cast<const int *>(smem + p.win_off) + R;
+        const int *ids_s = reinterpret_cast<const int *>(smem + p.win_off) + KMAX * kBM;   // the id window
 #pragma unroll
         for (int j = 0; j < kIdIters; ++j) {
             const int i = w0 + lane + 32 * j;
@@ -564,7 +580,8 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
     int *lst_k = reinterpret_cast<int *>(smem + p.exch_off);            // [NPART][KMAX][128] keys
     int *lst_i = lst_k + NPART * kBM * KMAX;                               // [NPART][KMAX][128] ids
     float *lst_rz = reinterpret_cast<float *>(lst_i + NPART * kBM * KMAX); // [NPART][2][128]
-    float *win_v = reinterpret_cast<float *>(smem + p.win_off);            // [KMAX][128]
+    float *win_v = reinterpret_cast<float *>(smem + p.win_off);            // [KMAX][128] logits, then weights
+    int *win_i = reinterpret_cast<int *>(win_v + KMAX * kBM);              // [KMAX][128] ids
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -728,7 +745,10 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
             int j = 0;
             for (int tile = first_tile; tile < p.tiles; tile += tile_step, ++j) {
                 const int b = j & 1;
-                if (!mbar_wait_bounded(&tail.acc_full[b], (j >> 1) & 1, abort_flag, 64)) break;
+                // (a vote, so that the warp leaves the wait together: lanes that left the
+                // polling loop at different times would otherwise run what follows apart)
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tail.acc_full[b], (j >> 1) & 1, abort_flag, 64)))
+                    break;
                 tc_fence_after_sync();
                 // ---- this part's columns: two interleaved lists for ILP
                 int ak[KMAX], bk[KMAX], ai[KMAX], bi[KMAX];
@@ -836,6 +856,7 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
                     const int *ok = lst_k + kOther * KMAX * kBM + row;
                     const int *oi = lst_i + kOther * KMAX * kBM + row;
                     float *wrow = win_v + row;
+                    int *irow = win_i + row;
                     int pa = 0, pb = 0;
 #pragma unroll 1
                     for (int k = 0; k < K; ++k) {
@@ -846,10 +867,8 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
                         const bool take_b = ranks_above(kb, ib, ka, ia);
                         wrow[k * kBM] = key_value(take_b ? kb : ka);
                         const int sel = take_b ? ib : ia;
-                        if (mine) {
-                            p.topk_idx[static_cast<int64_t>(n) * K + k] = sel;
-                            if (p.counts && sel < E) atomicAdd(hist_s + sel, 1);
-                        }
+                        irow[k * kBM] = sel;
+                        if (mine && p.counts && sel < E) atomicAdd(hist_s + sel, 1);
                         pa += take_b ? 0 : 1;
                         pb += take_b ? 1 : 0;
                     }
@@ -860,23 +879,31 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
                         const float r1 = lst_rz[(kOther * 2) * kBM + row], z1 = lst_rz[(kOther * 2 + 1) * kBM + row];
                         zfull = (z0 > 0.f ? z0 * expf(r0 - m) : 0.f) + (z1 > 0.f ? z1 * expf(r1 - m) : 0.f);
                     }
+                    // the window's logits become exp(logit - m), then the weights
                     float denom = zfull;
-                    if (p.renorm) {
-                        denom = 0.f;
+                    if (p.renorm) denom = 0.f;
 #pragma unroll 1
-                        for (int k = 0; k < K; ++k) denom += expf(wrow[k * kBM] - m);
+                    for (int k = 0; k < K; ++k) {
+                        const float e = expf(wrow[k * kBM] - m);
+                        wrow[k * kBM] = e;
+                        if (p.renorm) denom += e;
                     }
-                    if (mine) {
 #pragma unroll 1
-                        for (int k = 0; k < K; ++k)
-                            p.topk_w[static_cast<int64_t>(n) * K + k] = expf(wrow[k * kBM] - m) / denom;
-                        if (p.lse) p.lse[n] = m == -INFINITY ? -INFINITY : m + logf(zfull);
-                    }
+                    for (int k = 0; k < K; ++k) wrow[k * kBM] = wrow[k * kBM] / denom;
+                    if (mine && p.lse) p.lse[n] = m == -INFINITY ? -INFINITY : m + logf(zfull);
+                    // this quarter's tokens leave with coalesced stores (the warp holds them all)
+                    __syncwarp();
+                    const int r0 = q * 32;
+                    const int64_t n0 = static_cast<int64_t>(tile) * p.tile_rows + r0;
+                    const int64_t left = min(static_cast<int64_t>(p.tile_rows - r0), p.N - n0);
+                    const int vr = left <= 0 ? 0 : (left < 32 ? static_cast<int>(left) : 32);
+                    window_to_global<int>(p.topk_idx + n0 * K, win_i, r0, vr, K, lane, 32);
+                    window_to_global<float>(p.topk_w + n0 * K, win_v, r0, vr, K, lane, 32);
                 }
                 named_barrier_sync(1 + q, 32 * NPART);   // the lists have been consumed
             }
         } else {
-            acc_ok = mbar_wait_bounded(&tail.acc_full[0], 0, abort_flag, 64);
+            acc_ok = __all_sync(0xffffffffu, mbar_wait_bounded(&tail.acc_full[0], 0, abort_flag, 64));
             tc_fence_after_sync();
         }
     }
@@ -959,13 +986,13 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
                     }
 #pragma unroll
                 for (int u = 0; u < 8; u += 2) {
-                    topk_push<KMAX>(ak, ai, order_key(logit_of(x[u], bias_s[col + u * G])), col + u * G);
+                    topk_push<KMAX>(ak, ai, canon_key(canon_logit(x[u], bias_s[col + u * G])), col + u * G);
                     // (K > 8: one list, to stay within the registers of two CTAs per SM)
                     if constexpr (KMAX <= 8)
-                        topk_push<KMAX>(bk, bi, order_key(logit_of(x[u + 1], bias_s[col + (u + 1) * G])),
+                        topk_push<KMAX>(bk, bi, canon_key(canon_logit(x[u + 1], bias_s[col + (u + 1) * G])),
                                         col + (u + 1) * G);
                     else
-                        topk_push<KMAX>(ak, ai, order_key(logit_of(x[u + 1], bias_s[col + (u + 1) * G])),
+                        topk_push<KMAX>(ak, ai, canon_key(canon_logit(x[u + 1], bias_s[col + (u + 1) * G])),
                                         col + (u + 1) * G);
                 }
             }
@@ -975,7 +1002,7 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     if (c < nslices) x += rowbuf[c * sstride + col];
-                topk_push<KMAX>(ak, ai, order_key(logit_of(x, bias_s[col])), col);
+                topk_push<KMAX>(ak, ai, canon_key(canon_logit(x, bias_s[col])), col);
             }
             // K rounds of selection across the 2G lists of the token (warp shuffles
             // between its G threads); the winner's list drops its head
@@ -1002,12 +1029,8 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
                 topk_pop_if<KMAX>(bk, bi, bi[0] == i);
                 if (part == 0) {
                     wrow[k * kBM] = fv;
-                    // the dispatch tail's copy of the id: window rows R .. 2R - 1 are unused (S >= 2)
-                    if constexpr (FUSE) reinterpret_cast<int *>(wrow)[k * kBM + R] = i;
-                    if (n < p.N) {
-                        p.topk_idx[static_cast<int64_t>(n) * K + k] = i;
-                        if (p.counts && i < E) atomicAdd(hist_s + i, 1);
-                    }
+                    win_i[k * kBM + lrow] = i;   // also read by the dispatch tail
+                    if (n < p.N && p.counts && i < E) atomicAdd(hist_s + i, 1);
                 }
             }
             float z = 0.f;
@@ -1024,18 +1047,26 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
 #pragma unroll 1
                 for (int o = G >> 1; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
             }
-            if (part == 0 && n < p.N) {
-                float denom = z;
-                if (p.renorm) {
-                    denom = 0.f;
+            if (part == 0) {
+                // the window's logits become exp(logit - m), then the weights
+                float denom = p.renorm ? 0.f : z;
 #pragma unroll 1
-                    for (int k = 0; k < K; ++k) denom += expf(wrow[k * kBM] - m);
+                for (int k = 0; k < K; ++k) {
+                    const float e = expf(wrow[k * kBM] - m);
+                    wrow[k * kBM] = e;
+                    if (p.renorm) denom += e;
                 }
 #pragma unroll 1
-                for (int k = 0; k < K; ++k)
-                    p.topk_w[static_cast<int64_t>(n) * K + k] = expf(wrow[k * kBM] - m) / denom;
-                if (p.lse) p.lse[n] = m == -INFINITY ? -INFINITY : m + logf(z);
+                for (int k = 0; k < K; ++k) wrow[k * kBM] = wrow[k * kBM] / denom;
+                if (n < p.N && p.lse) p.lse[n] = m == -INFINITY ? -INFINITY : m + logf(z);
             }
+            // the CTA's R consecutive tokens leave with coalesced stores
+            named_barrier_sync(6, 32 * kEpiWarps);
+            const int64_t n0 = static_cast<int64_t>(first_tile) * p.tile_rows + static_cast<int64_t>(rank) * R;
+            const int64_t left = p.N - n0;
+            const int vr = left <= 0 ? 0 : (left < R ? static_cast<int>(left) : R);
+            window_to_global<int>(p.topk_idx + n0 * K, win_i, 0, vr, K, t, 32 * kEpiWarps);
+            window_to_global<float>(p.topk_w + n0 * K, win_v, 0, vr, K, t, 32 * kEpiWarps);
         }
     }
 
