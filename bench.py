@@ -588,21 +588,19 @@ def run_ours(args, rank, world, local):
         if rc:
             raise RuntimeError(f"a library call failed: {moe.status_string(rc)}")
 
-    def step_calls_timed(ev, fused):
-        """One step with an event pair around each call: [route, dispatch, combine], or
-        [route_dispatch, combine] for the one-launch call."""
+    def timed_calls(fn, n):
+        """Event times (ms) of n calls of fn, each alone: the L2 flushed before it, an
+        event pair around it on the launching stream, no other kernel in between."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
         rc = 0
-        calls = ([lambda: L.moe_route_dispatch(*fused_args)] if fused else
-                 [lambda: route_fn(*route_args), lambda: disp_fn(*disp_args)])
-        calls.append(lambda: comb_fn(*comb_args))
-        for j, c in enumerate(calls):
-            ev[j].record(stream)
-            rc |= c()
-        if stats_buf is not None and not fused:
-            rc |= L.moe_load_stats(vp(cnt_buf), E, vp(lse_buf), N, ctypes.c_float(1e-3), vp(stats_buf), sp)
-        ev[len(calls)].record(stream)
+        for i in range(n):
+            flush.zero_()
+            evs[i][0].record(stream)
+            rc |= fn()
+            evs[i][1].record(stream)
         if rc:
             raise RuntimeError(f"a library call failed: {moe.status_string(rc)}")
+        return evs
 
     # route + dispatch + combine; moe_dispatch copies rows in a launch of their own
     # once the copy moves 256 MiB or more (moe_dispatch_ep likewise for its send rows)
@@ -649,18 +647,22 @@ def run_ours(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     value = weak_scaling_tokens_per_s(world, N, args.steps, total_ms)
 
-    # ---- per-kernel durations for the roofline: the same steps with an event
-    # pair around every call (kernel time plus its own launch latency)
+    # ---- per-kernel durations for the roofline: every call of the step timed in a
+    # loop of its own (L2 flushed before each call, one event pair around it: the
+    # kernel's time plus its own launch latency).  Timing the calls interleaved
+    # inside whole steps instead read the router at the E=128 layer ~4 us slower
+    # than the router alone, an effect of the previous step's traffic rather than
+    # of the router's work.
     names = ["route", "dispatch", "combine"]
     ksteps = min(args.steps, 1000)
-    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ksteps)]
-    for i in range(ksteps):
-        flush.zero_()
-        step_calls_timed(kevs[i], False)
-    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(ksteps)] if fuse else []
-    for i in range(len(fevs)):
-        flush.zero_()
-        step_calls_timed(fevs[i], True)
+    calls = {"route": lambda: route_fn(*route_args), "dispatch": lambda: disp_fn(*disp_args),
+             "combine": lambda: comb_fn(*comb_args)}
+    if stats_buf is not None:
+        calls["load_stats"] = lambda: L.moe_load_stats(vp(cnt_buf), E, vp(lse_buf), N, ctypes.c_float(1e-3),
+                                                       vp(stats_buf), sp)
+    if fuse:
+        calls["route_dispatch"] = lambda: L.moe_route_dispatch(*fused_args)
+    kevs = {n: timed_calls(f, ksteps) for n, f in calls.items()}
     # ---- hot L2: the same steps with no flush in between (what fits in the
     # 129 MB L2 stays there from one step to the next)
     hevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ksteps)]
@@ -674,10 +676,7 @@ def run_ours(args, rank, world, local):
         time.sleep(0.2)
         sampler.stop()
     t2 = time.time()
-    per = {n: [ev[j].elapsed_time(ev[j + 1]) for ev in kevs] for j, n in enumerate(names)}
-    if fuse:
-        per["route_dispatch"] = [ev[0].elapsed_time(ev[1]) for ev in fevs]
-        per["combine_after_route_dispatch"] = [ev[1].elapsed_time(ev[2]) for ev in fevs]
+    per = {n: [ev[0].elapsed_time(ev[1]) for ev in evs] for n, evs in kevs.items()}
 
     # ---- the same step replayed from a CUDA graph (launch overhead removed)
     graph = None
@@ -820,7 +819,9 @@ def run_ours(args, rank, world, local):
                    "traffic": ncu_traffic(n, w.name)}
     if fuse:
         kern["route_dispatch"]["launches"] = fused_launches.value
-        kern["combine_after_route_dispatch_ms"] = statistics.fmean(per["combine_after_route_dispatch"])
+    if "load_stats" in per:
+        kern["load_stats"] = {"ms": statistics.fmean(per["load_stats"]),
+                              "median_ms": statistics.median(per["load_stats"])}
     # the roofline is that of the longest kernel of the timed step (the route +
     # dispatch call counts as a kernel only where it was one launch)
     step_kernels = ["route_dispatch", "combine"] if fuse and fused_launches.value == 1 else names
@@ -854,13 +855,13 @@ def run_ours(args, rank, world, local):
         "kernel_sum": {"tokens_per_s": N / (sum(kern[n]["median_ms"] for n in names) * 1e-3),
                        "ms": sum(kern[n]["median_ms"] for n in names),
                        "what": "N / (median route + median dispatch + median combine), each call timed alone "
-                               "with an event pair, L2 flushed before each step"},
+                               "with an event pair, L2 flushed before each call"},
         "load": {"max_over_mean": load[0], "p95_over_mean": load[1], "mean_slots_per_expert": load[3],
                  "over_ranks": world},
         "torch_naive": naive,
-        "timing": ("value: K steps, one event pair per step; kernels: a second pass of min(K,1000) "
-                   "steps with an event pair per call (route, dispatch and combine as separate calls; "
-                   "route_dispatch: the one call the step makes when fused)"),
+        "timing": ("value: K steps, one event pair per step; kernels: each call of the step (route, dispatch, "
+                   "combine as separate calls; route_dispatch: the one call the step makes when fused) timed "
+                   "alone in a loop of min(K,1000) calls, L2 flushed before each call, one event pair per call"),
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, residual=args.residual,
