@@ -99,6 +99,7 @@ struct TcParams {
     int need_z;            // the full softmax denominator is needed (renorm off, or lse requested)
     int EP, NP, stages, nsplit, kb_per, tiles;
     int tile_rows;         // tokens per tile (kBM, or fewer so that the tiles fill whole waves of SMs)
+    int kpack;             // persistent mode: K-steps per ring stage (1, or 2 with the 3D X map)
     uint32_t tmem_cols;
     uint32_t exch_off;     // byte offset of the epilogue exchange area (from the aligned base)
     uint32_t win_off;      // byte offset of the per-token winning logits
@@ -572,7 +573,7 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
     unsigned char *smem = smem_raw + smem_pad;
     const uint32_t b_slot_bytes = static_cast<uint32_t>(p.EP) * kBK * 2;
     unsigned char *a_base = smem;
-    unsigned char *b_base = smem + static_cast<size_t>(p.stages) * kABytes;
+    unsigned char *b_base = smem + static_cast<size_t>(p.stages) * kABytes * (SPLIT ? 1 : p.kpack);
     TcSmemTail &tail = *reinterpret_cast<TcSmemTail *>(smem + p.tail_off);
     float *bias_s = reinterpret_cast<float *>(&tail + 1);
     int *hist_s = reinterpret_cast<int *>(bias_s + p.EP);                // [EP] selections per expert
@@ -659,27 +660,44 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
     bool acc_ok = false;  // split mode, epilogue threads: the partial accumulator is complete
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // (the ring slot and its phase advance by counters: this thread paces the
+        // stream, so its loop is kept free of divisions)
         if (lane == 0) {
             const uint64_t pol_x = l2_policy_evict_first();
             const uint64_t pol_w = l2_policy_evict_last();
-            uint32_t g = 0;  // K-steps issued so far (across tiles)
+            const int kp = SPLIT ? 1 : p.kpack;   // K-steps per ring stage
+            const int nst = (nkb + kp - 1) / kp;   // ring stages per tile
+            const uint32_t stage_a = kABytes * kp, stage_b = b_slot_bytes * kp;
+            const int nwb = p.EP / 64;             // gate-weight boxes per stage
+            uint32_t g = 0, s = 0, ph = 0;         // stages issued (across tiles), ring slot, its phase
             bool stop = false;
             for (int tile = first_tile; tile < p.tiles && !stop; tile += tile_step) {
                 const int m0 = tile * p.tile_rows;
-                for (int i = 0; i < nkb; ++i) {
-                    const uint32_t s = g % p.stages;
-                    const uint32_t use = g / p.stages;
-                    if (!mbar_wait_bounded(&tail.empty[s], (use & 1u) ^ 1u, abort_flag)) {
+                for (int i = 0; i < nst; ++i) {
+                    if (!mbar_wait_bounded(&tail.empty[s], ph ^ 1u, abort_flag)) {
                         stop = true;
                         break;
                     }
-                    const int kb = kb0 + i;
-                    mbar_arrive_expect_tx(&tail.full[s], kABytes + b_slot_bytes);
-                    tma_load_2d(a_base + static_cast<size_t>(s) * kABytes, &tmX, &tail.full[s], kb * kBK, m0, pol_x);
-                    for (int j = 0; j < p.EP / 64; ++j)
-                        tma_load_2d(b_base + static_cast<size_t>(s) * b_slot_bytes + j * kBBoxBytes, &tmW,
-                                    &tail.full[s], j * 64, kb * kBK, pol_w);
+                    uint64_t *fb = &tail.full[s];
+                    unsigned char *as = a_base + s * stage_a;
+                    unsigned char *bs = b_base + s * stage_b;
+                    mbar_arrive_expect_tx(fb, stage_a + stage_b);
+                    if (kp == 1) {
+                        const int kc = (kb0 + i) * kBK;
+                        tma_load_2d(as, &tmX, fb, kc, m0, pol_x);
+                        for (int jw = 0; jw < nwb; ++jw) tma_load_2d(bs + jw * kBBoxBytes, &tmW, fb, jw * 64, kc, pol_w);
+                    } else {
+                        // two K-steps: one 3D box of X ([2 column blocks][kBM rows][64]) and one
+                        // [128 K-rows x 64 experts] box of the gate weight per 64 experts
+                        tma_load_3d(as, &tmX, fb, 0, m0, 2 * i, pol_x);
+                        for (int jw = 0; jw < nwb; ++jw)
+                            tma_load_2d(bs + jw * 2 * kBBoxBytes, &tmW, fb, jw * 64, 2 * i * kBK, pol_w);
+                    }
                     ++g;
+                    if (++s == static_cast<uint32_t>(p.stages)) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             if (*abort_flag) {
@@ -693,11 +711,19 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // (as the producer: counters for the ring, and descriptors of slot 0 to which a
+        // slot's byte offset >> 4 is added in the start-address field)
         if (lane == 0) {
             const uint32_t idesc = make_idesc_bf16_f32(kBM, static_cast<uint32_t>(p.NP), 0u, 1u);
-            const uint32_t a0 = smem_u32(a_base);
-            const uint32_t b0 = smem_u32(b_base);
-            uint32_t g = 0;
+            const int kp = SPLIT ? 1 : p.kpack;
+            const int nst = (nkb + kp - 1) / kp;
+            const uint32_t stage_a = kABytes * kp, stage_b = b_slot_bytes * kp;
+            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; +32 B per K=16 step, the
+            // next 64-column block kABytes further on.  B: MN-major, 64-expert atoms kp x 8 KiB
+            // apart (LBO), 8-row K groups 1024 B apart (SBO); +16 rows x 128 B per K=16 step.
+            const uint64_t a_desc0 = make_smem_desc_sw128(smem_u32(a_base), 16, 1024);
+            const uint64_t b_desc0 = make_smem_desc_sw128(smem_u32(b_base), kp * kBBoxBytes, 1024);
+            uint32_t s = 0, ph = 0;
             int j = 0;
             bool stop = false;
             for (int tile = first_tile; tile < p.tiles; tile += tile_step, ++j) {
@@ -705,27 +731,30 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
                 if (!mbar_wait_bounded(&tail.acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.NP);
-                for (int i = 0; i < nkb; ++i) {
-                    const uint32_t s = g % p.stages;
-                    const uint32_t use = g / p.stages;
-                    if (!mbar_wait_bounded(&tail.full[s], use & 1u, abort_flag)) {
+                for (int i = 0; i < nst; ++i) {
+                    if (!mbar_wait_bounded(&tail.full[s], ph, abort_flag)) {
                         stop = true;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a_s = a0 + s * kABytes;
-                    const uint32_t b_s = b0 + s * b_slot_bytes;
+                    const uint64_t ad = a_desc0 + ((s * stage_a) >> 4);
+                    const uint64_t bd = b_desc0 + ((s * stage_b) >> 4);
+                    const uint32_t acc0 = i != 0 ? 1u : 0u;
+                    if (kp == 1) {
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // A: K-major, 128-byte rows, 8-row groups 1024 B apart; +32 B per K=16 step
-                        const uint64_t a_desc = make_smem_desc_sw128(a_s + kk * 32, 16, 1024);
-                        // B: MN-major, 64-expert atoms 8 KiB apart (LBO), 8-row K groups 1024 B
-                        // apart (SBO); +16 rows x 128 B per K=16 step
-                        const uint64_t b_desc = make_smem_desc_sw128(b_s + kk * 2048, kBBoxBytes, 1024);
-                        tc_mma_f16(d_tmem, a_desc, b_desc, idesc, (i | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc_mma_f16(d_tmem, ad + kk * 2, bd + kk * 128, idesc, kk != 0 ? 1u : acc0);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 2 * (kBK / 16); ++kk)
+                            tc_mma_f16(d_tmem, ad + (kk >> 2) * (kABytes >> 4) + (kk & 3) * 2, bd + kk * 128, idesc,
+                                       kk != 0 ? 1u : acc0);
                     }
                     tc_commit(&tail.empty[s]);  // slot free once these MMAs have read it
-                    ++g;
+                    if (++s == static_cast<uint32_t>(p.stages)) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (stop) break;
                 tc_commit(&tail.acc_full[b]);   // this tile's logits (or partial logits) complete
@@ -1120,6 +1149,23 @@ bool encode_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// X [N, H] viewed as [H/64 column blocks][N rows][64]: a box of 2 blocks x rows x
+// 64 lands in shared memory as two [rows x 64] 128-byte-swizzled tiles back to
+// back, i.e. two K-steps of the A operand in one copy.  Needs H % 64 == 0 (so
+// that the blocks tile the rows exactly); false if the driver refuses the map.
+bool encode_x_3d(CUtensorMap *map, const void *base, uint64_t H, uint64_t N, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn || H % 64 != 0) return false;
+    const cuuint64_t dims[3] = {64, N, H / 64};
+    const cuuint64_t strides[2] = {H * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int kmax_for(int K) { return K <= 2 ? 2 : K <= 4 ? 4 : K <= 8 ? 8 : 16; }
 
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -1139,9 +1185,10 @@ struct TcLayout {
 // the staging area overlays the ring instead (it is written only once every
 // CTA of the cluster has finished its MMAs), for gates so wide that a ring
 // beside it would hold a single stage.
-bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, TcLayout &L, int nparts = 2)
+bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, TcLayout &L, int nparts = 2,
+                int kpack = 1)
 {
-    const size_t slot = kABytes + static_cast<size_t>(EP) * kBK * 2;
+    const size_t slot = (kABytes + static_cast<size_t>(EP) * kBK * 2) * kpack;
     const size_t staging = split ? static_cast<size_t>(kBM) * stage_row_floats(NP) * sizeof(float) : 0;
     const size_t apart = alias ? 0 : staging;
     const size_t exch = (split ? 0 : exch_lists_bytes(kmax, nparts)) + win_bytes(kmax);
@@ -1255,6 +1302,7 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     q.EP = (a.E + 63) / 64 * 64;
     q.NP = (a.E + 15) / 16 * 16;
     q.tiles = static_cast<int>((a.N + kBM - 1) / kBM);
+    q.kpack = 1;
     const int nk = (a.H + kBK - 1) / kBK;
 
     // split H over a cluster while the tiles alone leave SMs idle
@@ -1292,8 +1340,20 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
             q.tiles = static_cast<int>((a.N + rows - 1) / rows);
         }
     }
-    if (split ? !split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, L)
-              : !layout_for(q.EP, q.NP, KMAX, false, nk, false, L, TcShape<KMAX, false>::kParts))
+    // persistent mode: two K-steps per ring stage where the 3D view of X can be
+    // encoded (one X copy and one gate-weight copy per 64 experts bring 32 KiB of X).
+    // MOE_ROUTE_KPACK=1 (read once per process) keeps one K-step per stage.
+    CUtensorMap tmX3, tmW2;
+    static const bool kpack1 = [] {
+        const char *v = std::getenv("MOE_ROUTE_KPACK");
+        return v != nullptr && std::strcmp(v, "1") == 0;
+    }();
+    if (!split && !kpack1 && encode_x_3d(&tmX3, a.X, static_cast<uint64_t>(a.H), static_cast<uint64_t>(a.N), kBM) &&
+        encode_2d_bf16(&tmW2, a.W, static_cast<uint64_t>(a.E), static_cast<uint64_t>(a.H), 64, 2 * kBK) &&
+        layout_for(q.EP, q.NP, KMAX, false, nk, false, L, TcShape<KMAX, false>::kParts, 2) && L.stages >= 3)
+        q.kpack = 2;
+    if (q.kpack == 1 && (split ? !split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, L)
+                               : !layout_for(q.EP, q.NP, KMAX, false, nk, false, L, TcShape<KMAX, false>::kParts)))
         return cudaErrorInvalidConfiguration;
     q.stages = L.stages;
     q.exch_off = L.exch_off;
@@ -1374,6 +1434,7 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     }
     if (split) return cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, true>, tmX, tmW, q);
     if ((err = set_smem_attr<KMAX, false>(dev)) != cudaSuccess) return err;
+    if (q.kpack == 2) return cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, false>, tmX3, tmW2, q);
     return cudaLaunchKernelEx(&cfg, route_tc_kernel<KMAX, false>, tmX, tmW, q);
 }
 

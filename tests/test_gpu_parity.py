@@ -63,7 +63,11 @@ def gpu_fixture(Xp, counts, E):
 TC_SHAPES = [(1, 8, 8, 1), (7, 64, 16, 2), (129, 256, 16, 2), (300, 1024, 64, 4), (257, 512, 128, 8),
              (130, 2048, 256, 16), (65, 96, 48, 3), (33, 40, 24, 5), (200, 128, 8, 8), (513, 320, 32, 2),
              (1000, 4096, 64, 2), (20000, 128, 256, 16), (40000, 256, 64, 2), (25000, 512, 128, 8),
-             (30001, 256, 64, 4), (19457, 512, 32, 2), (1000, 7168, 256, 8)]
+             (30001, 256, 64, 4), (19457, 512, 32, 2), (1000, 7168, 256, 8),
+             # persistent mode with two K-steps per ring stage: an odd number of 64-column
+             # blocks (the last stage's second block is past H), E = 256 with K <= 8; and
+             # H % 64 != 0, which keeps one K-step per stage
+             (20001, 192, 64, 2), (24000, 4160, 64, 4), (20000, 1024, 256, 8), (21000, 200, 32, 2)]
 SIMT_ONLY_SHAPES = [(50, 64, 2, 2), (70, 128, 7, 3), (40, 256, 255, 8), (17, 24, 1, 1), (90, 512, 100, 6)]
 
 
