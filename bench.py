@@ -58,6 +58,10 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=mi.BENCH_WORKLOAD, choices=sorted(mi.WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--record-traffic", metavar="NCU_CSV", default=None,
+                   help="parse an ncu --csv launch log of this workload's step (metrics dram__bytes_read.sum, "
+                        "dram__bytes_write.sum) and write its per-call DRAM bytes into profiles/dram_traffic.csv, "
+                        "with the digest of each kernel's current source; runs nothing on a GPU")
     p.add_argument("--tokens", type=int, default=0,
                    help="run the workload's shape with this many tokens instead of its N (for profiler "
                         "captures on a smaller case; the line then names the workload NAME@N=T)")
@@ -144,6 +148,82 @@ def ncu_traffic(kernel: str, workload: str, path: str = None):
                 continue
             return value if r.get("source_digest") == source_digest(kernel) else None
     return None
+
+
+NCU_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+
+
+def ncu_launches(path: str):
+    """The launches of an ncu --csv log in launch order: [(kernel name, dram bytes read,
+    dram bytes written)], bytes converted from ncu's units."""
+    import csv
+    import io
+    with open(path, newline="") as f:
+        lines = f.read().splitlines()
+    start = next(i for i, ln in enumerate(lines) if ln.startswith('"ID"'))
+    per = {}
+    order = []
+    for r in csv.DictReader(io.StringIO("\n".join(lines[start:]))):
+        key = r["ID"]
+        if key not in per:
+            per[key] = {"name": r["Kernel Name"]}
+            order.append(key)
+        name = r["Metric Name"]
+        if name in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            per[key][name] = float(r["Metric Value"].replace(",", "")) * NCU_UNITS.get(r["Metric Unit"], 1)
+    return [(per[k]["name"], per[k].get("dram__bytes_read.sum"), per[k].get("dram__bytes_write.sum"))
+            for k in order]
+
+
+def record_traffic(ncu_csv: str, w: mi.Workload, path: str = None) -> dict:
+    """Per-call DRAM bytes of the step from an ncu launch log, written into the traffic table.
+
+    Each call's figure is the smallest over its captured launches (they agree to a fraction
+    of a percent); the dispatch call is its counting-sort launch plus, where the row copy runs
+    apart, the permute launch that follows it.  Returns {call: (read, write)}."""
+    import csv
+    path = path or TRAFFIC_FILE
+    calls = {}
+
+    def add(call, rd, wr):
+        if rd is None or wr is None:
+            return
+        if call not in calls or rd + wr < sum(calls[call]):
+            calls[call] = (rd, wr)
+
+    launches = ncu_launches(ncu_csv)
+    i = 0
+    while i < len(launches):
+        name, rd, wr = launches[i]
+        if "route_tc_kernel" in name:
+            add("route_dispatch" if ", 1, 1>" in name else "route", rd, wr)
+        elif "dispatch_fused_kernel" in name:
+            if i + 1 < len(launches) and "permute_kernel" in launches[i + 1][0]:
+                _, rd2, wr2 = launches[i + 1]
+                if None not in (rd, wr, rd2, wr2):
+                    add("dispatch", rd + rd2, wr + wr2)
+                i += 1
+            else:
+                add("dispatch", rd, wr)
+        elif "combine_kernel" in name:
+            add("combine", rd, wr)
+        i += 1
+    kb = kernel_bytes(w)
+    with open(path, newline="") as f:
+        rows = list(csv.DictReader(f))
+    fields = ["kernel", "workload", "dram_bytes_per_launch", "source_digest", "read", "write",
+              "algorithmic_bytes", "capture"]
+    rows = [r for r in rows if not (r["workload"] == w.name and r["kernel"] in calls)]
+    for call, (rd, wr) in sorted(calls.items()):
+        rows.append({"kernel": call, "workload": w.name, "dram_bytes_per_launch": int(rd + wr),
+                     "source_digest": source_digest(call), "read": int(rd), "write": int(wr),
+                     "algorithmic_bytes": kb[call],
+                     "capture": os.path.basename(ncu_csv) + " (bench.py --record-traffic)"})
+    with open(path, "w", newline="") as f:
+        wtr = csv.DictWriter(f, fieldnames=fields, lineterminator="\n")
+        wtr.writeheader()
+        wtr.writerows(rows)
+    return calls
 
 
 def max_over_ranks(value: float, dist_mod=None, device=None) -> float:
@@ -880,6 +960,10 @@ def main():
         name = f"{w.name}@N={args.tokens}"
         mi.WORKLOADS[name] = dataclasses.replace(w, name=name, N=args.tokens)
         args.workload = name
+    if args.record_traffic:
+        calls = record_traffic(args.record_traffic, mi.WORKLOADS[args.workload])
+        print(json.dumps({"recorded": args.workload, "calls": calls}))
+        return
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -155,3 +155,38 @@ def test_source_digest_ignores_comments_only():
     assert '"// kept"' in bench.code_only(a)
     for k in ("route", "dispatch", "combine", "route_dispatch"):
         assert len(bench.source_digest(k)) == 16
+
+
+def test_record_traffic_parses_an_ncu_log(tmp_path):
+    # the traffic table is written from ncu's own CSV log: per call the smallest of its
+    # launches, the dispatch call as its counting-sort launch plus the permute launch that
+    # follows it, units converted, every row stamped with the kernel source's digest
+    import bench
+    import moe_inputs as mi
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+           '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"')
+
+    def launch(i, name, rd, wr, unit="byte"):
+        row = f'"{i}","1","python3","h","{name}","1","7","(1, 1, 1)","(1, 1, 1)","0","10.3","m",'
+        return [row + f'"dram__bytes_read.sum","{unit}","{rd}"', row + f'"dram__bytes_write.sum","{unit}","{wr}"',
+                row + '"gpu__time_duration.sum","ns","1000"']
+
+    rows = ["==PROF== Connected", hdr]
+    rows += launch(0, "void route_tc_kernel<2, 0, 0>(CUtensorMap_st)", 1000, 10)
+    rows += launch(1, "void dispatch_fused_kernel<0, 0, 1>(FusedParams)", 5, 0)
+    rows += launch(2, "void permute_kernel<1, 0, 16>(const uint4 *)", 200, 400)
+    rows += launch(3, "void combine_kernel<2, 8, 0>(const uint4 *)", 0.5, 0.25, unit="Kbyte")
+    rows += launch(4, "void route_tc_kernel<2, 0, 0>(CUtensorMap_st)", 990, 10)
+    log = tmp_path / "launches.csv"
+    log.write_text("\n".join(rows) + "\n")
+    table = tmp_path / "traffic.csv"
+    table.write_text("kernel,workload,dram_bytes_per_launch,source_digest,read,write,algorithmic_bytes,capture\n"
+                     "route,other,1,x,1,0,1,old\n")
+    w = mi.WORKLOADS["tiny_n512_h256_e16_k2"]
+    calls = bench.record_traffic(str(log), w, str(table))
+    assert calls == {"route": (990.0, 10.0), "dispatch": (205.0, 400.0), "combine": (500.0, 250.0)}
+    assert bench.ncu_traffic("route", w.name, str(table)) == 1000.0
+    assert bench.ncu_traffic("dispatch", w.name, str(table)) == 605.0
+    assert bench.ncu_traffic("combine", w.name, str(table)) == 750.0
+    assert bench.ncu_traffic("route", "other", str(table)) is None      # digest "x" is not the source's
+    assert "route,other,1,x,1,0,1,old" in table.read_text()             # other workloads' rows kept
