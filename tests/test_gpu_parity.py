@@ -98,7 +98,9 @@ def test_route_tcgen05_rejects_unaligned_experts():
 
 
 @pytest.mark.parametrize("algo", ["tcgen05", "simt"])
-@pytest.mark.parametrize("N,H,E,K", [(200, 64, 16, 4), (300, 128, 64, 8), (129, 256, 128, 16), (77, 64, 8, 8)])
+@pytest.mark.parametrize("N,H,E,K", [(200, 64, 16, 4), (300, 128, 64, 8), (129, 256, 128, 16), (77, 64, 8, 8),
+                                     # persistent mode (two K-steps per ring stage)
+                                     (20000, 128, 128, 8), (19500, 256, 64, 4)])
 def test_route_integer_ties_exact(algo, N, H, E, K):
     # integer-valued operands: exact integer logits in fp32 too, with many ties,
     # so the lower-index rule must hold with no tolerance at all
@@ -112,8 +114,9 @@ def test_route_integer_ties_exact(algo, N, H, E, K):
 
 
 @pytest.mark.parametrize("algo", ["tcgen05", "simt"])
-def test_route_renorm_off_and_bias(algo):
-    N, H, E, K = 300, 512, 64, 4
+@pytest.mark.parametrize("N", [300, 20000])    # split mode, persistent mode
+def test_route_renorm_off_and_bias(algo, N):
+    H, E, K = 512, 64, 4
     X, W, _ = mi.make_route_inputs(N, H, E, seed=11)
     bias = mi.zipf_bias(E)
     for renorm in (True, False):
@@ -123,8 +126,9 @@ def test_route_renorm_off_and_bias(algo):
 
 
 @pytest.mark.parametrize("algo", ["tcgen05", "simt"])
-def test_route_nan_logit_is_minus_inf(algo):
-    N, H, E, K = 64, 128, 16, 16
+@pytest.mark.parametrize("N", [64, 20000])     # split mode, persistent mode
+def test_route_nan_logit_is_minus_inf(algo, N):
+    H, E, K = 128, 16, 16
     X, W, _ = mi.make_route_inputs(N, H, E, seed=12)
     bias = torch.zeros(E)
     bias[3] = float("nan")
