@@ -49,6 +49,17 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &r)
     }
 }
 
+// The output rows: streamed through L2 (evict-first), or, where the whole
+// output fits in L2 next to what is still in use (`keep`), stored with the
+// default write-back policy for the kernel that reads them next.
+__device__ __forceinline__ void st_out(uint4 *p, const uint4 &v, int keep)
+{
+    if (keep)
+        *p = v;
+    else
+        __stcs(p, v);
+}
+
 // KT > 0: K known at compile time -- every lane issues the loads of CPL
 // chunks x KT rows before the first FMA (CPL * KT <= 16 uint4 in flight per
 // lane).  KT == 0: runtime K, one chunk at a time.  RES: add residual[n,:]
@@ -57,7 +68,7 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &r)
 template <int KT, int CPL, bool RES>
 __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
     const uint4 *__restrict__ Y, const int32_t *__restrict__ row_map, const float *__restrict__ w, int64_t N,
-    int H, int K_rt, const uint4 *residual, uint4 *out, int32_t *status)
+    int H, int K_rt, const uint4 *residual, uint4 *out, int32_t *status, int keep)
 {
     const int K = KT > 0 ? KT : K_rt;
     const int warp = threadIdx.x >> 5;
@@ -108,7 +119,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
 #pragma unroll
                     for (int k = 0; k < KT; ++k) fma_bf16x8(acc, y[j][k], wk[k]);
                     if constexpr (RES) add_bf16x8(acc, rr[j]);
-                    if (c < chunks) __stcs(dst + c, pack_bf16x8(acc));
+                    if (c < chunks) st_out(dst + c, pack_bf16x8(acc), keep);
                 }
             }
         } else {
@@ -124,7 +135,7 @@ __global__ void __launch_bounds__(kCombWarps * 32) combine_kernel(
                 if constexpr (RES) {
                     if (v) add_bf16x8(acc, __ldcs(res + c));
                 }
-                if (v) __stcs(dst + c, pack_bf16x8(acc));
+                if (v) st_out(dst + c, pack_bf16x8(acc), keep);
             }
         }
     }
@@ -164,8 +175,9 @@ cudaError_t launch_combine_t(const void *Y, const int32_t *row_map, const float 
     const uint4 *res = static_cast<const uint4 *>(residual);
     uint4 *o = static_cast<uint4 *>(out);
     const int chunks = H / 8;
+    const int keep = keep_in_l2(N * 2 * static_cast<int64_t>(H), dev) ? 1 : 0;
 #define MOE_COMBINE_LAUNCH(KK, C) \
-    return cudaLaunchKernelEx(&cfg, combine_kernel<KK, C, RES>, y, row_map, w, N, H, K, res, o, status)
+    return cudaLaunchKernelEx(&cfg, combine_kernel<KK, C, RES>, y, row_map, w, N, H, K, res, o, status, keep)
     switch (K) {
     case 1:
         switch (pow2_chunks_per_lane(chunks, 16)) {

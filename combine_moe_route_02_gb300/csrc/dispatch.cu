@@ -333,11 +333,23 @@ __device__ __forceinline__ void quant_row_batch(const uint4 (&x)[CPL], uint2 (&q
     }
 }
 
+// Row stores: streamed through L2 (evict-first), or, where the whole output
+// fits in L2 next to what is still in use (`keep`), with the default
+// write-back policy, so that the kernel that reads the rows next finds them there.
+template <typename T>
+__device__ __forceinline__ void st_row(T *p, const T &v, int keep)
+{
+    if (keep)
+        *p = v;
+    else
+        __stcs(p, v);
+}
+
 template <bool kBf16Out, bool kFp8, int CPL>
 __device__ __forceinline__ void store_row_batch(const uint4 (&x)[CPL], const uint2 (&q)[kFp8 ? CPL : 1],
                                                 const float (&sc)[kFp8 ? CPL : 1], int base, int my_row, int K,
                                                 int H, uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq,
-                                                const ScaleOut Xs, int lane)
+                                                const ScaleOut Xs, int lane, int keep)
 {
     const int chunks = H >> 3;
     const int nb = H >> 7;
@@ -348,9 +360,9 @@ __device__ __forceinline__ void store_row_batch(const uint4 (&x)[CPL], const uin
         for (int j = 0; j < CPL; ++j) {
             const int c = base + lane + 32 * j;
             if (c >= chunks) continue;
-            if constexpr (kBf16Out) __stcs(Xp + static_cast<int64_t>(r) * chunks + c, x[j]);
+            if constexpr (kBf16Out) st_row(Xp + static_cast<int64_t>(r) * chunks + c, x[j], keep);
             if constexpr (kFp8) {
-                __stcs(reinterpret_cast<uint2 *>(Xq + static_cast<int64_t>(r) * H) + c, q[j]);
+                st_row(reinterpret_cast<uint2 *>(Xq + static_cast<int64_t>(r) * H) + c, q[j], keep);
                 if ((lane & 15) == 0) {
                     const int64_t at = static_cast<int64_t>(r) * nb + (c >> 4);
                     if (Xs.ue8m0)
@@ -371,7 +383,7 @@ __device__ __forceinline__ void store_row_batch(const uint4 (&x)[CPL], const uin
 template <bool kBf16Out, bool kFp8, int CPL>
 __device__ __forceinline__ void copy_token_rows(const uint4 *__restrict__ src, int my_row, int K, int H,
                                                 uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq,
-                                                const ScaleOut Xs, int lane)
+                                                const ScaleOut Xs, int lane, int keep)
 {
     const int chunks = H >> 3;  // 16-byte chunks per row
     for (int base = 0; base < chunks; base += 32 * CPL) {
@@ -380,14 +392,14 @@ __device__ __forceinline__ void copy_token_rows(const uint4 *__restrict__ src, i
         float sc[kFp8 ? CPL : 1];
         load_row_batch<CPL>(src, base, chunks, lane, x);
         quant_row_batch<kFp8, CPL>(x, q, sc, Xs.ue8m0);
-        store_row_batch<kBf16Out, kFp8, CPL>(x, q, sc, base, my_row, K, H, Xp, Xq, Xs, lane);
+        store_row_batch<kBf16Out, kFp8, CPL>(x, q, sc, base, my_row, K, H, Xp, Xq, Xs, lane, keep);
     }
 }
 
 template <bool kBf16Out, bool kFp8, int CPL>
 __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(
     const uint4 *__restrict__ X, const int32_t *__restrict__ row_map, int64_t N, int H, int K,
-    uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq, const ScaleOut Xs, int32_t *status, int skip_unset)
+    uint4 *__restrict__ Xp, uint8_t *__restrict__ Xq, const ScaleOut Xs, int32_t *status, int skip_unset, int keep)
 {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -406,7 +418,7 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(
                 my_row = -1;
             }
         }
-        copy_token_rows<kBf16Out, kFp8, CPL>(X + n * (H >> 3), my_row, K, H, Xp, Xq, Xs, lane);
+        copy_token_rows<kBf16Out, kFp8, CPL>(X + n * (H >> 3), my_row, K, H, Xp, Xq, Xs, lane, keep);
     }
     if (bad) report_status(status, MOE_ERR_BAD_INDEX);
     pdl_launch_dependents();
@@ -445,6 +457,7 @@ struct FusedParams {
     unsigned *bar;  // [0] arrive, [1] depart
     int32_t *hist;  // [gridDim.x][E]
     int ep_P;       // 0: keys are the expert ids; > 0: keys are EP ranks (E of them, ep_P experts each)
+    int keep;       // rows stored with the default write-back policy (they fit in L2), else streamed
 };
 
 struct FusedSmem {
@@ -709,10 +722,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) dispatch_fused_kernel(const 
         for (int j = warp; j < ntok; j += kFusedWarps) {
             const int my_row = lane < K ? rows_s[j * K + lane] : -1;
             if (j == warp && pre)
-                store_row_batch<kBf16Out, kFp8, CPL>(xpre, qpre, spre, 0, my_row, K, p.H, p.Xp, p.Xq, p.Xs, lane);
+                store_row_batch<kBf16Out, kFp8, CPL>(xpre, qpre, spre, 0, my_row, K, p.H, p.Xp, p.Xq, p.Xs, lane,
+                                                     p.keep);
             else
                 copy_token_rows<kBf16Out, kFp8, CPL>(p.X + (t0 + j) * chunks, my_row, K, p.H, p.Xp, p.Xq, p.Xs,
-                                                     lane);
+                                                     lane, p.keep);
         }
     }
 }
@@ -793,9 +807,11 @@ cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int
     const int chunks = H / 8;
     int cpl = chunks > 256 ? 16 : chunks > 128 ? 8 : chunks > 64 ? 4 : chunks > 32 ? 2 : 1;
     if (X_fp8 && cpl > 8) cpl = 8;  // codes and scales stay live too
+    const int64_t out_bytes = N * K * ((X_perm ? 2 * int64_t(H) : 0) + (X_fp8 ? int64_t(H) + H / 32 : 0));
+    const int keep = keep_in_l2(out_bytes, dev) ? 1 : 0;
 #define MOE_PERMUTE_LAUNCH(B, F, C) \
     return cudaLaunchKernelEx(&cfg, permute_kernel<B, F, C>, x, row_map, N, H, K, xp, xq, xs, status, \
-                              skip_unset ? 1 : 0)
+                              skip_unset ? 1 : 0, keep)
 #define MOE_PERMUTE_CPL8(B, F)                         \
     switch (cpl) {                                     \
     case 1: MOE_PERMUTE_LAUNCH(B, F, 1);               \
@@ -911,6 +927,7 @@ cudaError_t launch_dispatch_fused(const int32_t *topk_idx, const void *X, int64_
     p.bar = static_cast<unsigned *>(workspace);
     p.hist = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + 256);
     p.ep_P = ep_P;
+    p.keep = keep_in_l2(N * K * ((X_perm ? 2 * int64_t(H) : 0) + (X_fp8 ? int64_t(H) + H / 32 : 0)), dev) ? 1 : 0;
     const size_t slots = static_cast<size_t>(tok_per) * K;
     const size_t smem = sizeof(FusedSmem) + sizeof(int) * kFusedWarps * E + sizeof(int) * slots +
                         ((sizeof(uint16_t) * slots + 15) & ~size_t(15));

@@ -12,6 +12,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_cc_major[kMaxDevices];
+std::atomic<int64_t> g_l2_bytes[kMaxDevices];
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -49,6 +50,26 @@ int device_sm_count(int device)
         g_sm_count[d].store(v, std::memory_order_relaxed);
     }
     return v;
+}
+
+int64_t device_l2_bytes(int device)
+{
+    const int d = device & (kMaxDevices - 1);
+    int64_t v = g_l2_bytes[d].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        int b = 0;
+        if (cudaDeviceGetAttribute(&b, cudaDevAttrL2CacheSize, device) != cudaSuccess || b < 0) b = 0;
+        v = b > 0 ? b : 1;
+        g_l2_bytes[d].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+bool keep_in_l2(int64_t bytes, int device)
+{
+    // a little over half of the cache: what the next kernel reads back stays
+    // there next to the inputs still in use
+    return bytes <= device_l2_bytes(device) / 8 * 5;
 }
 
 int device_cc_major(int device)

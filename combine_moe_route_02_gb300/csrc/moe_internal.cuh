@@ -190,6 +190,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last()
 {
     uint64_t p;
@@ -456,5 +463,12 @@ moe_status dispatch_check(const int32_t *topk_idx, const void *X, int64_t N, int
 // Number of SMs of the current device (cached per device).
 int device_sm_count(int device);
 int device_cc_major(int device);
+// L2 size of a device in bytes (cached per device; 1 where the attribute is missing).
+int64_t device_l2_bytes(int device);
+// Whether a kernel's output of `bytes` is left in L2 for the kernel that reads it
+// next (default write-back stores, or the TMA's evict-normal policy for an input
+// that a later kernel reads again) rather than streamed through it (evict-first):
+// at most 5/8 of the L2.
+bool keep_in_l2(int64_t bytes, int device);
 
 }  // namespace moe

@@ -100,6 +100,8 @@ struct TcParams {
     int EP, NP, stages, nsplit, kb_per, tiles;
     int tile_rows;         // tokens per tile (kBM, or fewer so that the tiles fill whole waves of SMs)
     int kpack;             // persistent mode: K-steps per ring stage (1, or 2 with the 3D X map)
+    int x_keep;            // X fits in L2: its loads take the evict-normal policy (the row copy reads it
+                           // next), else evict-first
     uint32_t tmem_cols;
     uint32_t exch_off;     // byte offset of the epilogue exchange area (from the aligned base)
     uint32_t win_off;      // byte offset of the per-token winning logits
@@ -663,7 +665,7 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
         // (the ring slot and its phase advance by counters: this thread paces the
         // stream, so its loop is kept free of divisions)
         if (lane == 0) {
-            const uint64_t pol_x = l2_policy_evict_first();
+            const uint64_t pol_x = p.x_keep ? l2_policy_evict_normal() : l2_policy_evict_first();
             const uint64_t pol_w = l2_policy_evict_last();
             const int kp = SPLIT ? 1 : p.kpack;   // K-steps per ring stage
             const int nst = (nkb + kp - 1) / kp;   // ring stages per tile
@@ -1303,6 +1305,7 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     q.NP = (a.E + 15) / 16 * 16;
     q.tiles = static_cast<int>((a.N + kBM - 1) / kBM);
     q.kpack = 1;
+    q.x_keep = keep_in_l2(a.N * 2 * static_cast<int64_t>(a.H), dev) ? 1 : 0;
     const int nk = (a.H + kBK - 1) / kBK;
 
     // split H over a cluster while the tiles alone leave SMs idle
