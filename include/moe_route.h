@@ -221,8 +221,9 @@ MOE_API moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X,
  * whole path is ONE cooperative launch: each CTA, after its top-K epilogue,
  * counts its own slots, a bounded grid barrier follows, and every CTA then
  * forms the offsets, writes row_map for its slots and copies its tokens' rows
- * (from L2, where the router just streamed them).  Otherwise, or where the
- * cooperative launch is refused, the two calls run one after the other.
+ * (from L2, where the router just streamed them).  Otherwise (a row copy of
+ * more than 32 MiB included), or where the cooperative launch is refused, the
+ * two calls run one after the other.
  *   X, W_gate, bias, renorm, topk_idx, topk_w   as moe_route
  *   expert_counts, expert_offsets, row_map, src_slot   as moe_dispatch
  *   X_perm       bf16 [N*K, H], 16-byte aligned, or NULL (metadata only)
@@ -231,10 +232,11 @@ MOE_API moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X,
  *                that did not time out)
  *   launches     host int or NULL: out, the number of kernels this call launched
  * Errors: those of moe_route_ex and moe_dispatch_ex; MOE_ERR_WORKSPACE when the
- * workspace is missing or too small.  The status word receives
- * MOE_ERR_UNSUPPORTED (and no output is written) if a split-K launch did not
- * run in clusters of the planned size, MOE_ERR_TIMEOUT if the grid barrier ran
- * out (the workspace must then be zeroed before it is used again).
+ * workspace is missing or too small.  The status word receives MOE_ERR_TIMEOUT
+ * if the grid barrier ran out (the workspace must then be zeroed before it is
+ * used again).  A split-K launch whose clusters were dropped (a profiler may run
+ * a cooperative cluster launch that way) still gives the same outputs: each CTA
+ * then takes the whole H range of its tile and touches no other CTA's memory.
  * The one launch is cooperative.  With the environment variable
  * MOE_FUSED_LAUNCH=noncooperative (read once per process) it is launched
  * without that attribute, for profilers that run cooperative cluster launches
