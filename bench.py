@@ -10,8 +10,9 @@ inputs resident in HBM.  Prints ONE JSON line (rank 0).
 
 Timing: W untimed warm-up steps, then K timed steps.  Before every timed step
 a 256 MiB buffer is written to flush the 129 MB L2; each step is bracketed by
-CUDA events on the launching stream (the flush is outside the brackets), and
-every kernel of the step has its own event pair.  Under torchrun each rank
+CUDA events on the launching stream (the flush is outside the brackets); for
+the per-kernel figures every call of the step is also timed alone, the L2
+flushed before each call.  Under torchrun each rank
 runs its own replica on its own token batch (weak scaling, no collective on
 the data path); the reported time is the max over ranks.  Every rank shares one gate weight
 (the replica layout: tokens differ per rank, W_gate does not).

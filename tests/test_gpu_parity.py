@@ -651,7 +651,12 @@ ROUTE_DISPATCH_CASES = [
     (9000, 256, 64, 2, False, 1, 1),      # 71 tiles, clusters of 2
     (300, 7168, 64, 2, False, 1, 1),      # a CTA's rows do not fit in shared memory: copied from L2
     (1, 64, 8, 1, False, 2, 2),           # one K-step: no split, router and dispatch apart
-    (16384, 2048, 128, 8, False, 3, 2),   # persistent router
+    (16384, 2048, 128, 8, False, 3, 2),   # persistent router; 512 MiB of rows in a launch of their own
+    (65536, 256, 64, 2, True, 2, 2),      # persistent, four tiles per CTA, bias, renorm off
+    (20001, 192, 64, 2, False, 2, 2),     # persistent, ragged last tile, one K-step per stage
+    (30000, 512, 256, 16, False, 3, 2),   # persistent, E = 256, K = 16
+    (12000, 1024, 8, 1, False, 2, 2),     # persistent, E = 8, K = 1
+    (39912, 320, 64, 4, False, 2, 2),     # persistent, three tiles on most CTAs, two on the rest
     (300, 128, 12, 3, False, 2, 2),       # E % 8 != 0: CUDA-core router
 ]
 
