@@ -81,6 +81,16 @@ def test_route_matches_oracle(algo, N, H, E, K):
     print(algo, (N, H, E, K), stats)
 
 
+@pytest.mark.parametrize("N,H,E,K", [(600000, 64, 64, 2), (300001, 128, 128, 8)])
+def test_route_many_tiles_per_cta(N, H, E, K):
+    # persistent mode far past one wave: 31 and 16 tiles per CTA, so both TMEM
+    # accumulators and the ring's phases wrap many times; ragged last tile
+    X, W, bias = mi.make_route_inputs(N, H, E, seed=N + K, skew=True)
+    gi, gw = gpu_route(X, W, bias, K, algo="tcgen05")
+    oi, ow, L, P = oracle_route(X, W, bias, K)
+    compare_topk(gi, gw, oi, ow, L, P)
+
+
 @pytest.mark.parametrize("algo", ["simt", "auto"])
 @pytest.mark.parametrize("N,H,E,K", SIMT_ONLY_SHAPES)
 def test_route_simt_only_shapes(algo, N, H, E, K):
