@@ -23,6 +23,11 @@
  *    call and reads it after synchronising.  No kernel traps or asserts.
  *  - bf16 buffers are passed as `void*` (IEEE bfloat16 bit patterns).
  *  - Pointers must be 16-byte aligned; H must be a multiple of 8.
+ *  - Cache use: outputs that fit in 5/8 of the GPU's L2 (the row copies,
+ *    E4M3 codes and combine outputs) are stored with the default write-back
+ *    policy, so that the kernel that reads them next finds them in L2; larger
+ *    ones are streamed through it (evict-first).  The router leaves X in L2
+ *    the same way when X fits, for the row copy that reads it again.
  *
  * Notation: N tokens, H hidden size, E experts, K experts per token,
  * slot s = n*K + k.  Limits: 1 <= E <= 256, 1 <= K <= min(E, 16),
