@@ -227,7 +227,7 @@ MOE_API moe_status moe_dispatch_ex(const int32_t *topk_idx, const void *X,
  * counts its own slots, a bounded grid barrier follows, and every CTA then
  * forms the offsets, writes row_map for its slots and copies its tokens' rows
  * (from L2, where the router just streamed them).  Otherwise (a row copy of
- * more than 32 MiB included), or where the cooperative launch is refused, the
+ * more than 64 MiB included), or where the cooperative launch is refused, the
  * two calls run one after the other.
  *   X, W_gate, bias, renorm, topk_idx, topk_w   as moe_route
  *   expert_counts, expert_offsets, row_map, src_slot   as moe_dispatch

@@ -650,13 +650,14 @@ def test_graph_capture_replays_the_path():
 # ------------------------------------------------------------------ route + dispatch in one call
 
 # (N, H, E, K, bias+renorm off, launches with rows, launches metadata-only): split-mode
-# router shapes with a row copy of at most 32 MiB run as ONE launch; the others
+# router shapes with a row copy of at most 64 MiB run as ONE launch; the others
 # route and then dispatch (the row copy in a launch of its own from 256 MiB)
 ROUTE_DISPATCH_CASES = [
     (2048, 1024, 64, 2, False, 1, 1),     # the bench workload (clusters of 4)
     (512, 256, 16, 2, False, 1, 1),
     (4096, 512, 64, 4, False, 1, 1),
-    (4096, 2048, 64, 4, False, 2, 1),     # 64 MiB of rows: the dispatch kernel copies them
+    (4096, 2048, 64, 4, False, 1, 1),     # 64 MiB of rows: the largest copy inside the one launch
+    (4100, 2048, 64, 4, False, 2, 1),     # 4 tokens more: the dispatch kernel copies the rows
     (777, 512, 32, 3, True, 1, 1),        # ragged last tile, bias, renorm off
     (600, 2048, 256, 8, False, 1, 1),     # staging area overlaid on the TMA ring
     (1000, 7168, 256, 8, False, 2, 1),
