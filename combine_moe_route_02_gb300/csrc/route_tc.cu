@@ -540,17 +540,31 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
             }
             if (issued) bulk_commit_and_wait_all();
         } else {
+            // eight 16-byte chunks per lane loaded before any of them is stored (the
+            // stores may alias X as far as the compiler knows, so a plain loop would
+            // keep one load in flight)
+            constexpr int kCpl = 8;
             for (int j = warp; j < ntok; j += kWarps) {
                 const uint4 *src = p.d_X + (n0 + j) * chunks;
                 int rk[KMAX];
 #pragma unroll
                 for (int k = 0; k < KMAX; ++k) rk[k] = k < K ? rows_s[j * K + k] : -1;
-#pragma unroll 4
-                for (int ch = lane; ch < chunks; ch += 32) {
-                    const uint4 v = __ldg(src + ch);
+                for (int base = 0; base < chunks; base += 32 * kCpl) {
+                    uint4 v[kCpl];
 #pragma unroll
-                    for (int k = 0; k < KMAX; ++k)
-                        if (rk[k] >= 0) p.d_Xp[static_cast<int64_t>(rk[k]) * chunks + ch] = v;
+                    for (int u = 0; u < kCpl; ++u) {
+                        const int ch = base + lane + 32 * u;
+                        v[u] = ch < chunks ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kCpl; ++u) {
+                        const int ch = base + lane + 32 * u;
+                        if (ch < chunks) {
+#pragma unroll
+                            for (int k = 0; k < KMAX; ++k)
+                                if (rk[k] >= 0) p.d_Xp[static_cast<int64_t>(rk[k]) * chunks + ch] = v[u];
+                        }
+                    }
                 }
             }
         }
