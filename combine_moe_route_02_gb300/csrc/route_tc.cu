@@ -1207,7 +1207,7 @@ struct TcLayout {
 // CTA of the cluster has finished its MMAs), for gates so wide that a ring
 // beside it would hold a single stage.
 bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, TcLayout &L, int nparts = 2,
-                int kpack = 1)
+                int kpack = 1, bool wide = false)
 {
     const size_t slot = (kABytes + static_cast<size_t>(EP) * kBK * 2) * kpack;
     const size_t staging = split ? static_cast<size_t>(kBM) * stage_row_floats(NP) * sizeof(float) : 0;
@@ -1216,7 +1216,7 @@ bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, Tc
     const size_t fixed = 1024 + apart + exch + sizeof(TcSmemTail) + (sizeof(float) + sizeof(int)) * EP;
     const int max_st = split ? (kb_per < kMaxStages ? (kb_per < 1 ? 1 : kb_per) : kMaxStages) : kMaxStages;
     const int min_st = split ? 1 : 2;
-    const size_t budgets[2] = {split ? static_cast<size_t>(113 * 1024) : kSmemLimit, kSmemLimit};
+    const size_t budgets[2] = {split && !wide ? static_cast<size_t>(113 * 1024) : kSmemLimit, kSmemLimit};
     for (size_t budget : budgets) {
         for (int st = max_st; st >= min_st; --st) {
             size_t ring = static_cast<size_t>(st) * slot;
@@ -1239,12 +1239,12 @@ bool layout_for(int EP, int NP, int kmax, bool split, int kb_per, bool alias, Tc
 
 // Split-mode layout: the staging area apart from the ring unless that leaves
 // a one-stage ring for more than one K-step and the overlay does better.
-bool split_layout(int EP, int NP, int kmax, int kb_per, TcLayout &L)
+bool split_layout(int EP, int NP, int kmax, int kb_per, TcLayout &L, bool wide = false)
 {
-    const bool ok = layout_for(EP, NP, kmax, true, kb_per, false, L);
+    const bool ok = layout_for(EP, NP, kmax, true, kb_per, false, L, 2, 1, wide);
     if (ok && (L.stages > 1 || kb_per <= 1)) return true;
     TcLayout A;
-    if (layout_for(EP, NP, kmax, true, kb_per, true, A) && (!ok || A.stages > L.stages)) {
+    if (layout_for(EP, NP, kmax, true, kb_per, true, A, 2, 1, wide) && (!ok || A.stages > L.stages)) {
         L = A;
         return true;
     }
@@ -1377,6 +1377,15 @@ cudaError_t plan_and_launch(const RouteArgs &a, const CUtensorMap &tmX, const CU
     if (q.kpack == 1 && (split ? !split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, L)
                                : !layout_for(q.EP, q.NP, KMAX, false, nk, false, L, TcShape<KMAX, false>::kParts)))
         return cudaErrorInvalidConfiguration;
+    // route + dispatch with one CTA per SM: the layout may take the whole of shared
+    // memory, so that the CTA's rows of X fit beside the dispatch scratch and leave
+    // as bulk stores (the planned clusters must still all be resident at once)
+    if (fz && split && fz->X_perm != nullptr && static_cast<int64_t>(S) * q.tiles <= sms) {
+        TcLayout W;
+        if (split_layout(q.EP, q.NP, KMAX, (nk + S - 1) / S, W, true) && W.smem > L.smem &&
+            max_active_clusters<KMAX, true>(W.smem, S, dev) >= q.tiles)
+            L = W;
+    }
     q.stages = L.stages;
     q.exch_off = L.exch_off;
     q.win_off = L.win_off;
