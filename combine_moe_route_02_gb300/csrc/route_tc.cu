@@ -422,29 +422,41 @@ __device__ __forceinline__ void fused_dispatch_tail(const TcParams &p, unsigned 
         return;
     }
 
-    // expert totals and the rows of lower CTAs: thread (grp, e) sums table rows
-    // grp, grp + groups, ...; sixteen loads in flight before the first add
+    // expert totals and the rows of lower CTAs: thread (grp, four experts q) sums
+    // table rows grp, grp + groups, ... as 16-byte vectors (E % 8 == 0 on this
+    // path; rows are E ints apart), eight loads in flight before the first add
     {
-        const int groups = kThreads / E;   // >= 1 (E <= 256)
-        const int e = tid % E;
-        const int grp = tid / E;
+        const int nq = E >> 2;
+        const int groups = kThreads / nq;   // >= 5 (E <= 256)
+        const int q = tid % nq;
+        const int grp = tid / nq;
         if (grp < groups) {
-            int tot = 0, bef = 0;
-            for (int c0 = grp; c0 < static_cast<int>(G); c0 += 16 * groups) {
-                int v[16];
+            const int4 *tab = reinterpret_cast<const int4 *>(p.d_hist);
+            int tot[4] = {0, 0, 0, 0}, bef[4] = {0, 0, 0, 0};
+            for (int c0 = grp; c0 < static_cast<int>(G); c0 += 8 * groups) {
+                int4 v[8];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < 8; ++u) {
                     const int cc = c0 + u * groups;
-                    v[u] = cc < static_cast<int>(G) ? __ldcg(p.d_hist + static_cast<int64_t>(cc) * E + e) : 0;
+                    v[u] = cc < static_cast<int>(G) ? __ldcg(tab + static_cast<int64_t>(cc) * nq + q)
+                                                     : make_int4(0, 0, 0, 0);
                 }
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    tot += v[u];
-                    bef += (c0 + u * groups < c) ? v[u] : 0;
+                for (int u = 0; u < 8; ++u) {
+                    const bool lower = c0 + u * groups < c;
+                    const int w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        tot[t] += w4[t];
+                        bef[t] += lower ? w4[t] : 0;
+                    }
                 }
             }
-            atomicAdd(&total[e], tot);
-            atomicAdd(&before[e], bef);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                atomicAdd(&total[4 * q + t], tot[t]);
+                atomicAdd(&before[4 * q + t], bef[t]);
+            }
         }
     }
     __syncthreads();
