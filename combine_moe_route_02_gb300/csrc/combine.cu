@@ -176,7 +176,8 @@ cudaError_t launch_combine_t(const void *Y, const int32_t *row_map, const float 
     uint4 *o = static_cast<uint4 *>(out);
     const int chunks = H / 8;
     const int keep = keep_in_l2(N * 2 * static_cast<int64_t>(H), dev) ? 1 : 0;
-#define MOE_COMBINE_LAUNCH(KK, C) \
+#define MOE_COMBINE_LAUNCH(KK, C)                                                              \
+    if ((err = prefer_l1_carveout<combine_kernel<KK, C, RES>>(dev)) != cudaSuccess) return err; \
     return cudaLaunchKernelEx(&cfg, combine_kernel<KK, C, RES>, y, row_map, w, N, H, K, res, o, status, keep)
     switch (K) {
     case 1:

@@ -809,7 +809,8 @@ cudaError_t launch_permute(const void *X, const int32_t *row_map, int64_t N, int
     if (X_fp8 && cpl > 8) cpl = 8;  // codes and scales stay live too
     const int64_t out_bytes = N * K * ((X_perm ? 2 * int64_t(H) : 0) + (X_fp8 ? int64_t(H) + H / 32 : 0));
     const int keep = keep_in_l2(out_bytes, dev) ? 1 : 0;
-#define MOE_PERMUTE_LAUNCH(B, F, C) \
+#define MOE_PERMUTE_LAUNCH(B, F, C)                                                            \
+    if ((err = prefer_l1_carveout<permute_kernel<B, F, C>>(dev)) != cudaSuccess) return err; \
     return cudaLaunchKernelEx(&cfg, permute_kernel<B, F, C>, x, row_map, N, H, K, xp, xq, xs, status, \
                               skip_unset ? 1 : 0, keep)
 #define MOE_PERMUTE_CPL8(B, F)                         \
@@ -841,6 +842,7 @@ cudaError_t launch_fused_t(const FusedParams &p, int grid, size_t smem, cudaStre
         if (err != cudaSuccess) return err;
         configured.fetch_or(bit);
     }
+    if ((err = prefer_l1_carveout<dispatch_fused_kernel<B, F, C>>(dev)) != cudaSuccess) return err;
     int occ = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dispatch_fused_kernel<B, F, C>, kFusedThreads, smem);
     if (err != cudaSuccess) return err;

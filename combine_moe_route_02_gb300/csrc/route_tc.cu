@@ -661,14 +661,16 @@ __global__ void __launch_bounds__(TcShape<KMAX, SPLIT>::kThr, SPLIT ? 2 : 1)
         tmem_alloc(&tail.tmem_base, p.tmem_cols);
         tmem_relinquish();
     }
-    // One wave of CTAs: the next kernel in the stream may start launching now
-    // (it still waits for this grid to complete before it reads anything).
-    // With the dispatch fused in there is no trigger at all: CTAs of the next
-    // kernel (the combine) placed on an SM that still holds one of these CTAs run
-    // with its large shared-memory carve-out, i.e. a small L1 to hold their loads
-    // in flight (at 4096 tokens the step took 54.2 instead of 50.3 us with the
-    // trigger at the end of this launch).
-    if constexpr (!FUSE) pdl_launch_dependents();
+    // No early launch trigger (griddepcontrol.launch_dependents): the next
+    // kernel in the stream is released when this grid completes.  An early
+    // trigger gained nothing in a stream, and in a CUDA graph it staged the next
+    // launch while these CTAs held every SM: the router itself then ran ~2 us
+    // longer at 16384 x 2048 x 128 experts, and the next kernels' CTAs ran with
+    // this kernel's large shared-memory carve-out, i.e. a small L1 for their
+    // loads in flight (graph replay of the 65536 x 4096 step: 644 against 586 us
+    // without the trigger).  With the dispatch fused in, the combine that follows
+    // was likewise slower with a trigger at the end of the launch (4096 tokens:
+    // 54.2 against 50.3 us per step).
     tc_fence_before_sync();
     __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after_sync();
