@@ -830,6 +830,39 @@ def test_graph_capture_replays_route_dispatch():
         assert torch.equal(out, ref_out) and torch.equal(d.X_perm, ref_rows) and torch.equal(d.row_map, ref_map)
 
 
+def test_graph_capture_replays_the_persistent_path():
+    # the E=128 layer's launch sequence in a CUDA graph: the persistent router, the
+    # counting-sort launch, the bf16 + E4M3 row copy in a launch of its own (512 MiB of
+    # rows), the combine; replays on their own stream reproduce the eager results
+    w = mi.WORKLOADS["moe_layer_n16384_h2048_e128_k8_fp8"]
+    X, W, _ = mi.make_route_inputs(w.N, w.H, w.E, 3)
+    Xd, Wd = X.to(DEV), W.to(DEV)
+    idx, tw = moe.route(Xd, Wd, w.K)
+    d = moe.dispatch(idx, w.E, Xd, fp8=True)
+    Y = gpu_fixture(d.X_perm, d.expert_counts, w.E)
+    out = moe.combine(Y, d.row_map, tw)
+    torch.cuda.synchronize()
+    outs = (idx, tw, d.expert_counts, d.expert_offsets, d.row_map, d.src_slot, d.X_perm, d.X_fp8, d.X_scale, out)
+    ref = [t.clone() for t in outs]
+    s = torch.cuda.Stream()
+    ws = torch.zeros(moe.dispatch_workspace_size(w.N, w.E, w.K), dtype=torch.uint8, device=DEV)
+    st = status_word()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            moe.route(Xd, Wd, w.K, topk_idx=idx, topk_w=tw, status=st, stream=s)
+            moe.dispatch(idx, w.E, Xd, fp8=True, out=d, workspace=ws, status=st, stream=s)
+            moe.combine(Y, d.row_map, tw, out=out, status=st, stream=s)
+    for _ in range(2):
+        for t in outs:
+            t.view(torch.uint8).zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert st.item() == 0, moe.status_string(st.item())
+        for got, want in zip(outs, ref):
+            assert torch.equal(got.view(torch.uint8), want.view(torch.uint8))
+
+
 # ------------------------------------------------------------------ seeded random shapes
 
 def _random_shapes(count, seed=2026):
