@@ -879,7 +879,23 @@ def _random_shapes(count, seed=2026):
     return shapes
 
 
-@pytest.mark.parametrize("N,H,E,K,skew,renorm", _random_shapes(64))
+def _random_persistent_shapes(count, seed=2027):
+    # token counts that put the tensor-core router in its persistent mode (more tiles
+    # than one split-K wave), with at most 2^26 elements of permuted rows
+    rng = np.random.default_rng(seed)
+    shapes = []
+    while len(shapes) < count:
+        E = int(rng.choice([8, 16, 24, 32, 64, 96, 128, 192, 256]))
+        K = int(rng.integers(1, min(E, 16) + 1))
+        H = int(rng.choice([64, 136, 320, 1024]))
+        N = int(rng.choice([10000, 14000, 20001, 27000, 39999]))
+        if N * K * H > 1 << 26:
+            continue
+        shapes.append((N, H, E, K, bool(rng.integers(0, 2)), bool(rng.integers(0, 2))))
+    return shapes
+
+
+@pytest.mark.parametrize("N,H,E,K,skew,renorm", _random_shapes(64) + _random_persistent_shapes(12))
 def test_random_shapes_whole_path_match_oracle(N, H, E, K, skew, renorm):
     # route (auto implementation), dispatch with rows, route + dispatch as one call, and the
     # combine, on shapes drawn across the supported range (E % 8 != 0 takes the CUDA-core router)
