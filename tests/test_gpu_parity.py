@@ -70,7 +70,10 @@ TC_SHAPES = [(1, 8, 8, 1), (7, 64, 16, 2), (129, 256, 16, 2), (300, 1024, 64, 4)
              (20001, 192, 64, 2), (24000, 4160, 64, 4), (20000, 1024, 256, 8), (21000, 200, 32, 2),
              # persistent mode with one tile per SM (fewer than 128 tokens each)
              (15000, 512, 64, 2), (12001, 320, 256, 16), (10000, 192, 64, 3), (19456, 2048, 128, 8),
-             (9730, 64, 192, 5)]
+             (9730, 64, 192, 5),
+             # persistent mode with K = E: each half of the expert columns holds fewer
+             # candidates than K, so the lists end in empty slots before the halves merge
+             (20000, 64, 8, 8), (20000, 128, 16, 16), (20000, 256, 24, 13)]
 SIMT_ONLY_SHAPES = [(50, 64, 2, 2), (70, 128, 7, 3), (40, 256, 255, 8), (17, 24, 1, 1), (90, 512, 100, 6)]
 
 
